@@ -1,0 +1,11 @@
+"""Latent-routed top-k SwiGLU MoE layer forward on B300 (sm_103a).
+
+The compute lives in libmoe.so (C ABI, include/moe.h); this package holds its
+CUDA sources (csrc/), the build script and a thin ctypes binding.
+"""
+from .binding import (  # noqa: F401
+    MoeError, MoeLayer, alloc_workspace, header_functions, lib, moe_check_dims, moe_clear_device_status,
+    moe_combine, moe_dims, moe_dispatch, moe_expert_ffn, moe_forward, moe_forward_host,
+    moe_get_device_status, moe_prepare_weights, moe_route, moe_scratch_size, moe_workspace_size,
+    moe_workspace_size_host, status_string,
+)

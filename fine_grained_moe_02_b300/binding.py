@@ -1,0 +1,248 @@
+"""ctypes binding of libmoe (include/moe.h), same names as the C entry points.
+
+Argument marshalling only: every step of the layer runs in libmoe's CUDA
+kernels.  Tensors are torch tensors on the current CUDA device (PyTorch is
+used for device memory and streams); they are passed as raw pointers.  If
+libmoe.so is missing or cannot be loaded the binding raises instead of
+falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import torch
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "libmoe.so"
+HEADER = PKG.parent / "include" / "moe.h"
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED_SHAPE = -2
+MOE_ERR_MISALIGNED = -3
+MOE_ERR_WORKSPACE_TOO_SMALL = -4
+MOE_ERR_CUDA = -5
+MOE_ERR_DEVICE_STATUS = -6
+MOE_ERR_TIMEOUT = -7
+MOE_DEV_BAD_EXPERT_ID = 0x1
+MOE_DEV_TIMEOUT = 0x2
+MOE_DEV_BAD_OFFSETS = 0x4
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("E", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("top_k", ctypes.c_int32)]
+
+    @classmethod
+    def make(cls, T, d, E, inter, top_k=6, n_heads=12, head_dim=256):
+        return cls(int(T), int(d), int(n_heads), int(head_dim), int(E), int(inter), int(top_k))
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_P = ctypes.c_void_p
+_DP = ctypes.POINTER(moe_dims)
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_check_dims": (ctypes.c_int, [_DP]),
+    "moe_scratch_size": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_workspace_size": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_workspace_size_host": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_clear_device_status": (ctypes.c_int, [_P, _P]),
+    "moe_get_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "moe_prepare_weights": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
+    "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_dispatch": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_expert_ffn": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_combine": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P]),
+    "moe_forward": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_host": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+}
+
+_lib = None
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/moe.h."""
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libmoe.so (built by fine_grained_moe_02_b300.build); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m fine_grained_moe_02_b300.build`")
+        L = ctypes.CDLL(str(LIB_PATH))
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def _ptr(t) -> ctypes.c_void_p | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(*ts, dtype=None) -> None:
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("expected a CUDA tensor")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"expected {dtype}, got {t.dtype}")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def moe_check_dims(dims: moe_dims) -> int:
+    return lib().moe_check_dims(ctypes.byref(dims))
+
+
+def moe_scratch_size(dims: moe_dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_scratch_size(ctypes.byref(dims), ctypes.byref(n)), "moe_scratch_size")
+    return n.value
+
+
+def moe_workspace_size(dims: moe_dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(dims), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_workspace_size_host(dims: moe_dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_host(ctypes.byref(dims), ctypes.byref(n)), "moe_workspace_size_host")
+    return n.value
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A uint8 device buffer for use as `ws` (PyTorch owns the memory)."""
+    return torch.zeros(int(nbytes), dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_clear_device_status(ws, stream=None) -> None:
+    _check(lib().moe_clear_device_status(_ptr(ws), _stream(stream)), "moe_clear_device_status")
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    rc = lib().moe_get_device_status(_ptr(ws), ctypes.byref(v), _stream(stream))
+    if rc not in (MOE_OK, MOE_ERR_DEVICE_STATUS):
+        _check(rc, "moe_get_device_status")
+    return v.value
+
+
+def moe_prepare_weights(dims, w_gate, w_up, w13, stream=None) -> None:
+    _dev(w_gate, w_up, w13, dtype=torch.bfloat16)
+    _check(lib().moe_prepare_weights(ctypes.byref(dims), _ptr(w_gate), _ptr(w_up), _ptr(w13), _stream(stream)),
+           "moe_prepare_weights")
+
+
+def moe_route(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _dev(x, w_lat, w_head, dtype=torch.bfloat16)
+    _dev(bias, topk_gate, logits, dtype=torch.float32)
+    _dev(topk_idx, dtype=torch.int32)
+    _check(lib().moe_route(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(topk_idx),
+                           _ptr(topk_gate), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def moe_dispatch(dims, x, topk_idx, offsets, row_of, src_token, x_perm, ws, stream=None) -> None:
+    _dev(x, x_perm, dtype=torch.bfloat16)
+    _dev(topk_idx, offsets, row_of, src_token, dtype=torch.int32)
+    _check(lib().moe_dispatch(ctypes.byref(dims), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
+                              _ptr(src_token), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def moe_expert_ffn(dims, x_perm, offsets, w13, w_down, act, y_perm, ws, stream=None) -> None:
+    _dev(x_perm, w13, w_down, act, y_perm, dtype=torch.bfloat16)
+    _dev(offsets, dtype=torch.int32)
+    _check(lib().moe_expert_ffn(ctypes.byref(dims), _ptr(x_perm), _ptr(offsets), _ptr(w13), _ptr(w_down),
+                                _ptr(act), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(dims, y_perm, row_of, topk_gate, out, stream=None) -> None:
+    _dev(y_perm, out, dtype=torch.bfloat16)
+    _dev(row_of, dtype=torch.int32)
+    _dev(topk_gate, dtype=torch.float32)
+    _check(lib().moe_combine(ctypes.byref(dims), _ptr(y_perm), _ptr(row_of), _ptr(topk_gate), _ptr(out),
+                             _stream(stream)), "moe_combine")
+
+
+def moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws, stream=None) -> None:
+    _dev(x, w_lat, w_head, w13, w_down, out, dtype=torch.bfloat16)
+    _dev(bias, dtype=torch.float32)
+    _check(lib().moe_forward(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(w13),
+                             _ptr(w_down), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(dims, x_host, w_lat, w_head, bias, w13, w_down, out_host, ws, stream=None) -> None:
+    """x_host/out_host: CPU bf16 tensors (pinned for full bandwidth); weights on the device."""
+    if x_host.is_cuda or out_host.is_cuda:
+        raise ValueError("x_host/out_host must be host tensors")
+    _dev(w_lat, w_head, w13, w_down, dtype=torch.bfloat16)
+    _dev(bias, dtype=torch.float32)
+    _check(lib().moe_forward_host(ctypes.byref(dims), _ptr(x_host), _ptr(w_lat), _ptr(w_head), _ptr(bias),
+                                  _ptr(w13), _ptr(w_down), _ptr(out_host), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "moe_forward_host")
+
+
+class MoeLayer:
+    """Device-resident weights plus a workspace; forward() runs moe_forward."""
+
+    def __init__(self, dims: moe_dims, w_lat, w_head, bias, w_gate, w_up, w_down, device="cuda"):
+        self.dims = dims
+        dev = torch.device(device)
+        self.w_lat = w_lat.to(dev)
+        self.w_head = w_head.to(dev)
+        self.bias = None if bias is None else bias.to(dev, torch.float32)
+        self.w_down = w_down.to(dev)
+        wg, wu = w_gate.to(dev), w_up.to(dev)
+        self.w13 = torch.empty((dims.E, 2 * dims.inter, dims.d), dtype=torch.bfloat16, device=dev)
+        moe_prepare_weights(dims, wg, wu, self.w13)
+        del wg, wu
+        self.ws = alloc_workspace(moe_workspace_size(dims), dev)
+
+    def forward(self, x, out=None, stream=None):
+        if out is None:
+            out = torch.empty((self.dims.T, self.dims.d), dtype=torch.bfloat16, device=x.device)
+        moe_forward(self.dims, x, self.w_lat, self.w_head, self.bias, self.w13, self.w_down, out, self.ws, stream)
+        return out
+
+    def device_status(self, stream=None) -> int:
+        return moe_get_device_status(self.ws, stream)

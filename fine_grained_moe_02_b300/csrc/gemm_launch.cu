@@ -1,0 +1,162 @@
+// Host launchers for the tcgen05 GEMM engine: the two router GEMMs and the
+// two grouped expert GEMMs, plus the tensor-map encoder and the w13 builder.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "epilogues.cuh"
+#include "gemm_tc.cuh"
+#include "internal.h"
+#include "moe.h"
+
+namespace moe {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+template <int BN, class Epi>
+int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& shape, const typename Epi::Params& ep,
+             int grid, cudaStream_t stream) {
+  using S = GemmSmem<BN>;
+  auto kern = gemm_tc_kernel<BN, Epi>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynBytes) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (grid < 1) grid = 1;
+  kern<<<grid, kGemmThreads, S::kDynBytes, stream>>>(ta, tb, shape, ep);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <class Epi>
+int run_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& shape,
+                const typename Epi::Params& ep, int grid, cudaStream_t stream) {
+  switch (bn) {
+    case 256: return run_gemm<256, Epi>(ta, tb, shape, ep, grid, stream);
+    case 128: return run_gemm<128, Epi>(ta, tb, shape, ep, grid, stream);
+    case 64: return run_gemm<64, Epi>(ta, tb, shape, ep, grid, stream);
+    case 32: return run_gemm<32, Epi>(ta, tb, shape, ep, grid, stream);
+    case 16: return run_gemm<16, Epi>(ta, tb, shape, ep, grid, stream);
+    default: return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+}
+
+int pick_bn(int n) {
+  if (n % 256 == 0) return 256;
+  if (n % 128 == 0) return 128;
+  return 64;
+}
+
+}  // namespace
+
+bool make_tmap_bf16_2d(void* tmap, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                       uint32_t box_rows) {
+  auto enc = encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Router: stage 1  hl = [hi | lo](x W_lat^T)            dense GEMM, N = L, fused hi/lo split
+//         stage 2  s  = hl [W_head | W_head]^T + bias   dense GEMM, K = 2L, N = E, fused top-k
+int launch_route(const RouteArgs& a, cudaStream_t stream) {
+  const int64_t m_tiles = (a.T + kBM - 1) / kBM;
+  CUtensorMap ta, tb;
+  {
+    const int bn = pick_bn(a.L);
+    if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, kBM)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&tb, a.w_lat, a.d, a.L, kBK, bn)) return MOE_ERR_CUDA;
+    GemmShape sh{a.d, a.d, a.L, 1, nullptr, static_cast<int>(a.T), a.status};
+    EpiHiLo::Params ep{a.hl, 2LL * a.L, a.L};
+    const int64_t tiles = m_tiles * (a.L / bn);
+    const int grid = static_cast<int>(tiles < a.sm_count ? tiles : a.sm_count);
+    const int rc = run_gemm_bn<EpiHiLo>(bn, ta, tb, sh, ep, grid, stream);
+    if (rc != MOE_OK) return rc;
+  }
+  {
+    const int bn = a.E <= 16 ? 16 : a.E <= 32 ? 32 : a.E <= 64 ? 64 : a.E <= 128 ? 128 : 256;
+    if (!make_tmap_bf16_2d(&ta, a.hl, 2ULL * a.L, a.T, kBK, kBM)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&tb, a.w_head, a.L, a.E, kBK, bn)) return MOE_ERR_CUDA;
+    GemmShape sh{2 * a.L, a.L, bn, 1, nullptr, static_cast<int>(a.T), a.status};
+    EpiTopK::Params ep{a.bias, a.logits, a.topk_idx, a.topk_gate, a.E, a.k};
+    const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
+    return run_gemm_bn<EpiTopK>(bn, ta, tb, sh, ep, grid, stream);
+  }
+}
+
+// Expert GEMMs over ragged groups (device offsets): GEMM-1 + SwiGLU, GEMM-2.
+int launch_ffn(const FfnArgs& a, cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  const int rows = static_cast<int>(a.rows);
+  {
+    const int n = 2 * a.I;
+    const int bn = (n % 256 == 0) ? 256 : 128;
+    if (!make_tmap_bf16_2d(&ta, a.x_perm, a.d, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
+    GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status};
+    EpiSwiGLU::Params ep{a.act, a.I};
+    const int rc = (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream)
+                               : run_gemm<128, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream);
+    if (rc != MOE_OK) return rc;
+  }
+  {
+    const int bn = pick_bn(a.d);
+    if (!make_tmap_bf16_2d(&ta, a.act, a.I, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, bn)) return MOE_ERR_CUDA;
+    GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
+    EpiStoreBf16::Params ep{a.y_perm, a.d};
+    return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, sh, ep, a.sm_count, stream);
+  }
+}
+
+// w13[e, 128b + j] = j < 64 ? w_gate[e, 64b + j] : w_up[e, 64b + j - 64]   (rows of d)
+__global__ void __launch_bounds__(256) prepare_w13_kernel(const uint4* __restrict__ wg, const uint4* __restrict__ wu,
+                                                          uint4* __restrict__ w13, int64_t n_rows, int I,
+                                                          int d_vec) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t r = wid; r < n_rows; r += nw) {       // r = e * 2I + row
+    const int64_t e = r / (2 * I);
+    const int row = static_cast<int>(r - e * 2 * I);
+    const int b = row >> 7, j = row & 127;
+    const uint4* src = (j < 64 ? wg : wu) + (e * I + b * 64 + (j & 63)) * d_vec;
+    uint4* dst = w13 + r * d_vec;
+    for (int c = lane; c < d_vec; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w13, int E, int I, int d,
+                       cudaStream_t stream) {
+  const int64_t n_rows = static_cast<int64_t>(E) * 2 * I;
+  const int64_t want = (n_rows + 7) / 8;
+  const int grid = static_cast<int>(want < 4096 ? want : 4096);
+  prepare_w13_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(w_gate),
+                                               reinterpret_cast<const uint4*>(w_up), reinterpret_cast<uint4*>(w13),
+                                               n_rows, I, d / 8);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

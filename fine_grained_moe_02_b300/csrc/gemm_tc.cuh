@@ -1,0 +1,300 @@
+// Persistent tcgen05 GEMM engine for sm_103a: D = A * B^T over ragged row
+// groups, bf16 operands, fp32 accumulation in tensor memory.
+//
+//   A: rows of a [M_total, K] bf16 matrix, loaded by TMA (128-byte swizzle)
+//   B: rows of a [groups * N, K_B] bf16 matrix (group g uses rows g*N ..),
+//      the k coordinate of B is k mod K_B (lets one B serve a K = c*K_B sweep)
+//   groups: device offsets[G + 1]; group g owns A rows [offsets[g], offsets[g+1])
+//
+// One CTA per SM, 192 threads:
+//   warp 0       TMA producer (one lane): fills a STAGES-deep shared-memory ring
+//   warp 1       MMA issuer (one lane) and TMEM owner: tcgen05.mma 128 x BN x 16
+//   warps 2..5   epilogue: tcgen05.ld the accumulator, apply Epi, store to HBM
+// The accumulator is double-buffered in TMEM so the epilogue of tile i
+// overlaps the main loop of tile i+1.  Tiles are handed out statically
+// (tile = blockIdx.x + i * gridDim.x) in group-major, m-major, n-minor order
+// so that CTAs running at the same time share A and B tiles through L2.
+//
+// Every wait is bounded (see ptx::mbar_wait): on a timeout the kernel sets
+// MOE_DEV_TIMEOUT in the status word, the other roles stop, in-flight TMA
+// loads and MMAs are drained (again with a limit), TMEM is freed and the
+// kernel returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "moe.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128;          // tile rows (UMMA M)
+constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of bf16
+constexpr int kUK = 16;           // k per tcgen05.mma (kind::f16)
+constexpr int kMaxGroups = 256;
+constexpr int kGemmThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct GemmShape {
+  int K;            // reduction length (A's columns)
+  int K_B;          // B's columns; B's k coordinate is k % K_B
+  int N;            // output columns per group (multiple of BN)
+  int groups;       // number of row groups (1 for a dense GEMM)
+  const int* offsets;  // device [groups + 1], or nullptr: one group of rows [0, M)
+  int M;            // rows when offsets == nullptr; row capacity of A otherwise
+  int* status;      // device status word
+};
+
+template <int BN>
+struct GemmSmem {
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
+  static constexpr int kAccStride = kTmemCols / 2;  // column offset of accumulator buffer 1
+  // ring + 1 KB slack for the manual 1024-byte alignment
+  static constexpr int kDynBytes = kStages * kStageBytes + 1024;
+};
+
+struct TileCoord {
+  int group, m_blk, n_blk;
+  int row0;      // first A row of the tile
+  int row_end;   // end of the group's rows (exclusive)
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, const int* s_tile, int groups,
+                                                 int n_tiles) {
+  // largest g with s_tile[g] <= tile
+  int lo = 0, hi = groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tile[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  TileCoord c;
+  c.group = lo;
+  const int local = tile - s_tile[lo];
+  c.m_blk = local / n_tiles;
+  c.n_blk = local - c.m_blk * n_tiles;
+  c.row0 = s_row[lo] + c.m_blk * kBM;
+  c.row_end = s_row[lo + 1];
+  return c;
+}
+
+// Epi must provide:
+//   struct Params;
+//   template <int BN> static __device__ void run(const Params&, const TileCoord&, uint32_t taddr,
+//                                                 int row_in_tile, int N);
+// taddr addresses this thread's lane (= tile row) at the accumulator's column 0.
+template <int BN, class Epi>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+               GemmShape shape, typename Epi::Params ep) {
+  using S = GemmSmem<BN>;
+  constexpr int STAGES = S::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int s_row[kMaxGroups + 1];
+  __shared__ int s_tile[kMaxGroups + 1];
+  __shared__ int s_total;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles = shape.N / BN;
+  const int groups = shape.groups;
+
+  // ---- group table: row offsets and tile prefix (all threads, then warp 0 scans)
+  for (int i = threadIdx.x; i <= groups; i += blockDim.x)
+    s_row[i] = shape.offsets ? __ldg(shape.offsets + i) : (i == 0 ? 0 : shape.M);
+  if (threadIdx.x == 0) s_abort = 0;
+  __syncthreads();
+  if (warp == 0) {
+    // per-group m-tile counts, validated; exclusive scan by one warp
+    bool bad = false;
+    int carry = 0;
+    for (int base = 0; base < groups; base += 32) {
+      const int g = base + lane;
+      int cnt = 0;
+      if (g < groups) {
+        const int a = s_row[g], b = s_row[g + 1];
+        if (a < 0 || b < a || b > shape.M) bad = true;
+        else cnt = ((b - a + kBM - 1) / kBM) * n_tiles;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < groups) s_tile[g] = carry + incl - cnt;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      s_tile[groups] = carry;
+      s_total = bad ? 0 : carry;
+      if (bad && blockIdx.x == 0) atomicOr(shape.status, MOE_DEV_BAD_OFFSETS);
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
+      ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 128);
+    }
+    ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&s_tmem), S::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_a);
+    ptx::prefetch_tmap(&tmap_b);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  const uint32_t tmem_base = s_tmem;
+  const int total = s_total;
+  const int num_kb = shape.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint64_t pol_a = ptx::policy_evict_normal();
+      const uint64_t pol_b = ptx::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0;       // bit s: stage s was filled at least once
+      uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
+        const int b_row = c.group * shape.N + c.n_blk * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
+          ptx::mbar_arrive_expect_tx(fb, S::kStageBytes);
+          const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
+          const uint32_t sb = sa + S::kABytes;
+          const int k = kb * kBK;
+          ptx::tma_load_2d(sa, &tmap_a, k, c.row0, fb, pol_a);
+          ptx::tma_load_2d(sb, &tmap_b, k % shape.K_B, b_row, fb, pol_b);
+          filled |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (!ok) {
+        atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        s_abort = 1;
+      }
+      // drain: every issued load must have landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s) {
+        if (filled & (1u << s)) {
+          const volatile int never = 0;
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, kWaitLimitNs))
+            atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = ptx::idesc_bf16_m128(BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), acc_phase ^ 1, &s_abort, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::kAccStride);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, &s_abort, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
+          const uint32_t sb = sa + S::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / kUK; ++kk) {
+            const uint64_t da = ptx::sw128_desc(sa + kk * kUK * 2);
+            const uint64_t db = ptx::sw128_desc(sb + kk * kUK * 2);
+            ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_u32(&tfull_bar[acc]));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      if (!ok) {
+        atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        s_abort = 1;
+      }
+      // drain: all MMAs issued by this thread complete before TMEM is freed
+      ptx::mma_commit(ptx::smem_u32(&drain_bar));
+      const volatile int never = 0;
+      if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, &never, kWaitLimitNs))
+        atomicOr(shape.status, MOE_DEV_TIMEOUT);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const bool ok = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+      const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
+      Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile,
+                            shape.N);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[acc]));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+}  // namespace moe

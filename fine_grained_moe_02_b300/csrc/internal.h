@@ -1,0 +1,78 @@
+// Internal interface between the C-ABI layer (moe_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+
+struct DispatchArgs {
+  const uint16_t* x;
+  const int32_t* topk_idx;
+  int64_t T;
+  int d, k, E;
+  int32_t* offsets;
+  int32_t* row_of;
+  int32_t* src_token;
+  uint16_t* x_perm;        // nullptr: permutation only
+  int32_t* block_counts;   // scratch [nblk * E]
+  int32_t* block_base;     // scratch [nblk * E]
+  int* status;
+  int sm_count;
+};
+
+struct RouteArgs {
+  const uint16_t* x;
+  const uint16_t* w_lat;
+  const uint16_t* w_head;
+  const float* bias;
+  int32_t* topk_idx;
+  float* topk_gate;
+  float* logits;
+  uint16_t* hl;            // scratch [T, 2L] bf16: latent hi | lo
+  int64_t T;
+  int d, L, E, k;
+  int* status;
+  int sm_count;
+};
+
+struct FfnArgs {
+  const uint16_t* x_perm;
+  const int32_t* offsets;
+  const uint16_t* w13;
+  const uint16_t* w_down;
+  uint16_t* act;
+  uint16_t* y_perm;
+  int64_t rows;            // T * k
+  int d, I, E;
+  int* status;
+  int sm_count;
+};
+
+struct CombineArgs {
+  const uint16_t* y_perm;
+  const int32_t* row_of;
+  const float* gate;
+  uint16_t* out;
+  int64_t T;
+  int d, k;
+  int sm_count;
+};
+
+int launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
+size_t dispatch_scratch_bytes(int64_t T, int E);
+int launch_route(const RouteArgs& a, cudaStream_t stream);
+int launch_ffn(const FfnArgs& a, cudaStream_t stream);
+int launch_combine(const CombineArgs& a, cudaStream_t stream);
+int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w13, int E, int I, int d,
+                       cudaStream_t stream);
+
+// cuTensorMapEncodeTiled, resolved once through the runtime (no -lcuda).
+bool make_tmap_bf16_2d(void* tmap /* CUtensorMap* */, const void* base, uint64_t cols, uint64_t rows,
+                       uint32_t box_cols, uint32_t box_rows);
+
+}  // namespace moe

@@ -1,0 +1,328 @@
+// C-ABI entry points of libmoe (declared in include/moe.h): argument checks,
+// workspace layout and the order of the stages on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "internal.h"
+#include "moe.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Scratch layout (offsets from ws):
+//   [0, 1024)                  status word (int32 at 0)
+//   dispatch counters          2 * nblk * E int32
+//   hl                         T * 2L bf16 (router latent hi | lo)
+struct ScratchLayout {
+  size_t disp, hl, end;
+};
+
+ScratchLayout scratch_layout(const moe_dims* d) {
+  ScratchLayout s;
+  const size_t L = static_cast<size_t>(d->n_heads) * d->head_dim;
+  s.disp = kAlign;
+  s.hl = align_up(s.disp + dispatch_scratch_bytes(d->T, d->E), kAlign);
+  s.end = align_up(s.hl + static_cast<size_t>(d->T) * 2 * L * 2, kAlign);
+  return s;
+}
+
+// Forward layout: scratch, then the layer's intermediates.  y_perm aliases
+// x_perm (x_perm is dead once expert GEMM-1 has run).
+struct ForwardLayout {
+  ScratchLayout s;
+  size_t idx, gate, offsets, row_of, src, xperm, act, end;
+};
+
+ForwardLayout forward_layout(const moe_dims* d) {
+  ForwardLayout f;
+  f.s = scratch_layout(d);
+  const size_t Tk = static_cast<size_t>(d->T) * d->top_k;
+  f.idx = f.s.end;
+  f.gate = align_up(f.idx + Tk * 4, kAlign);
+  f.offsets = align_up(f.gate + Tk * 4, kAlign);
+  f.row_of = align_up(f.offsets + (static_cast<size_t>(d->E) + 1) * 4, kAlign);
+  f.src = align_up(f.row_of + Tk * 4, kAlign);
+  f.xperm = align_up(f.src + Tk * 4, kAlign);
+  f.act = align_up(f.xperm + Tk * d->d * 2, kAlign);
+  f.end = align_up(f.act + Tk * d->inter * 2, kAlign);
+  return f;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int* status_ptr(void* ws) { return static_cast<int*>(ws); }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_STATUS: return "MOE_ERR_DEVICE_STATUS";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_check_dims(const moe_dims* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 1 || d->d < 1 || d->n_heads < 1 || d->head_dim < 1 || d->E < 1 || d->inter < 1 || d->top_k < 1)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int64_t L = static_cast<int64_t>(d->n_heads) * d->head_dim;
+  if (d->d % 64 != 0 || d->inter % 64 != 0 || L % 256 != 0 || L > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->E > kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->top_k > kMaxTopK || d->top_k > d->E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->T * d->top_k >= (static_cast<int64_t>(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(d->E) * 2 * d->inter >= (static_cast<int64_t>(1) << 31) ||
+      static_cast<int64_t>(d->E) * d->d >= (static_cast<int64_t>(1) << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int moe_scratch_size(const moe_dims* dims, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  const int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  *bytes = scratch_layout(dims).end;
+  return MOE_OK;
+}
+
+int moe_workspace_size(const moe_dims* dims, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  const int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  *bytes = forward_layout(dims).end;
+  return MOE_OK;
+}
+
+int moe_workspace_size_host(const moe_dims* dims, size_t* bytes) {
+  size_t b = 0;
+  const int rc = moe_workspace_size(dims, &b);
+  if (rc != MOE_OK) return rc;
+  const size_t io = align_up(static_cast<size_t>(dims->T) * dims->d * 2, kAlign);
+  *bytes = b + 2 * io;
+  return MOE_OK;
+}
+
+int moe_clear_device_status(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  return cudaMemsetAsync(ws, 0, sizeof(int), static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK
+                                                                                                : MOE_ERR_CUDA;
+}
+
+int moe_get_device_status(void* ws, int32_t* status, void* stream) {
+  if (ws == nullptr || status == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return v == 0 ? MOE_OK : MOE_ERR_DEVICE_STATUS;
+}
+
+int moe_prepare_weights(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
+                        void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (w_gate == nullptr || w_up == nullptr || w13 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w13)) return MOE_ERR_MISALIGNED;
+  return launch_prepare_w13(w_gate, w_up, w13, dims->E, dims->inter, dims->d, static_cast<cudaStream_t>(stream));
+}
+
+int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+              const float* bias, int32_t* topk_idx, float* topk_gate, float* logits, void* ws, size_t ws_bytes,
+              void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || topk_idx == nullptr || topk_gate == nullptr ||
+      ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(topk_idx) || !aligned16(topk_gate) ||
+      !aligned16(ws) || (bias != nullptr && !aligned16(bias)) || (logits != nullptr && !aligned16(logits)))
+    return MOE_ERR_MISALIGNED;
+  const ScratchLayout sl = scratch_layout(dims);
+  if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  RouteArgs a{};
+  a.x = x;
+  a.w_lat = w_lat;
+  a.w_head = w_head;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_gate = topk_gate;
+  a.logits = logits;
+  a.hl = at<uint16_t>(ws, sl.hl);
+  a.T = dims->T;
+  a.d = dims->d;
+  a.L = dims->n_heads * dims->head_dim;
+  a.E = dims->E;
+  a.k = dims->top_k;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_route(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx, int32_t* offsets,
+                 int32_t* row_of, int32_t* src_token, moe_bf16* x_perm, void* ws, size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || topk_idx == nullptr || offsets == nullptr || row_of == nullptr || src_token == nullptr ||
+      x_perm == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(offsets) || !aligned16(row_of) ||
+      !aligned16(src_token) || !aligned16(x_perm) || !aligned16(ws))
+    return MOE_ERR_MISALIGNED;
+  const ScratchLayout sl = scratch_layout(dims);
+  if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int64_t nblk_e = static_cast<int64_t>(dispatch_scratch_bytes(dims->T, dims->E) / 8);
+  DispatchArgs a{};
+  a.x = x;
+  a.topk_idx = topk_idx;
+  a.T = dims->T;
+  a.d = dims->d;
+  a.k = dims->top_k;
+  a.E = dims->E;
+  a.offsets = offsets;
+  a.row_of = row_of;
+  a.src_token = src_token;
+  a.x_perm = x_perm;
+  a.block_counts = at<int32_t>(ws, sl.disp);
+  a.block_base = at<int32_t>(ws, sl.disp) + nblk_e;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_dispatch(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets, const moe_bf16* w13,
+                   const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm, void* ws, size_t ws_bytes,
+                   void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w_down == nullptr || act == nullptr ||
+      y_perm == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(offsets) || !aligned16(w13) || !aligned16(w_down) || !aligned16(act) ||
+      !aligned16(y_perm) || !aligned16(ws))
+    return MOE_ERR_MISALIGNED;
+  if (ws_bytes < scratch_layout(dims).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  FfnArgs a{};
+  a.x_perm = x_perm;
+  a.offsets = offsets;
+  a.w13 = w13;
+  a.w_down = w_down;
+  a.act = act;
+  a.y_perm = y_perm;
+  a.rows = dims->T * dims->top_k;
+  a.d = dims->d;
+  a.I = dims->inter;
+  a.E = dims->E;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_ffn(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row_of, const float* topk_gate,
+                moe_bf16* out, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (y_perm == nullptr || row_of == nullptr || topk_gate == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(row_of) || !aligned16(topk_gate) || !aligned16(out))
+    return MOE_ERR_MISALIGNED;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  CombineArgs a{};
+  a.y_perm = y_perm;
+  a.row_of = row_of;
+  a.gate = topk_gate;
+  a.out = out;
+  a.T = dims->T;
+  a.d = dims->d;
+  a.k = dims->top_k;
+  a.sm_count = sms;
+  return launch_combine(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws,
+                size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
+      out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  const ForwardLayout f = forward_layout(dims);
+  if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
+  int32_t* idx = at<int32_t>(ws, f.idx);
+  float* gate = at<float>(ws, f.gate);
+  int32_t* offsets = at<int32_t>(ws, f.offsets);
+  int32_t* row_of = at<int32_t>(ws, f.row_of);
+  int32_t* src = at<int32_t>(ws, f.src);
+  moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
+  moe_bf16* act = at<moe_bf16>(ws, f.act);
+  if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_ffn(dims, xperm, offsets, w13, w_down, act, xperm, ws, ws_bytes, stream)) != MOE_OK)
+    return rc;
+  return moe_combine(dims, xperm, row_of, gate, out, stream);
+}
+
+int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* w_lat, const moe_bf16* w_head,
+                     const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out_host, void* ws,
+                     size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x_host == nullptr || out_host == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
+  size_t need = 0, inner = 0;
+  moe_workspace_size_host(dims, &need);
+  moe_workspace_size(dims, &inner);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const size_t io_bytes = static_cast<size_t>(dims->T) * dims->d * 2;
+  const size_t io = align_up(io_bytes, kAlign);
+  moe_bf16* x_dev = at<moe_bf16>(ws, inner);
+  moe_bf16* out_dev = at<moe_bf16>(ws, inner + io);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(x_dev, x_host, io_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((rc = moe_forward(dims, x_dev, w_lat, w_head, bias, w13, w_down, out_dev, ws, inner, stream)) != MOE_OK)
+    return rc;
+  if (cudaMemcpyAsync(out_host, out_dev, io_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+/*
+ * moe.h - C ABI of libmoe: forward pass of a latent-routed, top-k,
+ * fine-grained SwiGLU Mixture-of-Experts layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer (MagiMoE as described for MAGI-2 Preview):
+ *   - "MAGI-2 Preview" (heyaiwiki), Architecture table, "Routing" row and the
+ *     FAQ answer "What is MagiMoE?": multi-head latent routing with 12 latent
+ *     heads of 256 dims and top-6 expert selection over ultra-fine-grained
+ *     experts.
+ *   - "Sand.ai: The world's first 100-billion-parameter open-source MoE video
+ *     generation model MAGI Preview" (36kr), section "02. Two Key Technical
+ *     Decision Points": an operator library covering expert routing, sorting
+ *     and calculation, fusing steps to cut intermediate results and memory
+ *     traffic, tuned for many small matrix products.
+ * The pages fix only the head count, head dim and top-k; the arithmetic this
+ * library implements is:
+ *   h      = W_lat x                              (latent projection, [L] = [n_heads*head_dim])
+ *   s[e]   = sum_j <h_j, W_head[e, head j]> + b[e] (every head scores every expert; scores summed)
+ *   p      = softmax(s) over all E experts
+ *   idx    = the top_k experts by p, ties to the lowest expert index,
+ *            slot order: p descending then index ascending
+ *   gate_i = p[idx_i] / sum_j p[idx_j]
+ *   y_e    = W_down[e] (silu(W_gate[e] x) * (W_up[e] x))
+ *   out    = sum_i gate_i * y_{idx_i}  (slot order, fp32 accumulate, one bf16 rounding)
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except
+ *     where a name ends in _host.  The library never allocates device memory.
+ *   - Matrices are row-major.  Weights are stored [out, in] ("K-major").
+ *   - bf16 tensors are passed as moe_bf16 (the 16-bit pattern); fp32 as float.
+ *   - Every tensor pointer and the workspace must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     enqueue work on it and return without synchronising the host, except
+ *     moe_get_device_status, moe_forward_host (which ends with a stream sync)
+ *     and the size queries, which launch nothing.
+ *   - Arguments are checked on the host first; a failed check returns a
+ *     negative moe_status and launches nothing.  A CUDA launch error returns
+ *     MOE_ERR_CUDA.  Problems found on the device (an expert id outside
+ *     [0, E), inconsistent group offsets, a pipeline wait that ran past its
+ *     time limit) never trap: the offending row or tile is skipped and a
+ *     bit is OR-ed into a sticky device status word kept in the workspace;
+ *     read it with moe_get_device_status.
+ *   - Shape rules: T >= 1, d % 64 == 0, inter % 64 == 0, n_heads*head_dim %
+ *     256 == 0, 1 <= E <= 256, 1 <= top_k <= min(8, E), T*top_k < 2^31.
+ *   - Group sizes stay on the device; no entry point reads them back, so a
+ *     whole moe_forward can be enqueued without host synchronisation.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* bfloat16 bit pattern */
+
+/* Layer dimensions.  n_heads = 12, head_dim = 256, top_k = 6 for MagiMoE. */
+typedef struct moe_dims {
+  int64_t T;        /* tokens in the batch */
+  int32_t d;        /* hidden size */
+  int32_t n_heads;  /* latent routing heads */
+  int32_t head_dim; /* dims per latent head */
+  int32_t E;        /* routed experts */
+  int32_t inter;    /* expert intermediate size */
+  int32_t top_k;    /* experts per token */
+} moe_dims;
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* NULL pointer, negative size, bad enum */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* dims outside the shape rules above */
+  MOE_ERR_MISALIGNED = -3,         /* a pointer is not 16-byte aligned */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+  MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_STATUS = -6,      /* moe_get_device_status found a nonzero word */
+  MOE_ERR_TIMEOUT = -7             /* reserved: host-side wait gave up */
+} moe_status;
+
+/* Bits of the sticky device status word. */
+#define MOE_DEV_BAD_EXPERT_ID 0x1  /* topk_idx held an id outside [0, E); that slot was skipped */
+#define MOE_DEV_TIMEOUT 0x2        /* a pipeline wait exceeded its limit; that kernel stopped early */
+#define MOE_DEV_BAD_OFFSETS 0x4    /* group offsets not monotone / out of range; no tile was run */
+
+/* Human-readable name of a moe_status value.  Never NULL. */
+const char* moe_status_string(int status);
+
+/* Validates dims against the shape rules.  Pure host function. */
+int moe_check_dims(const moe_dims* dims);
+
+/* Bytes of scratch workspace needed by the stage calls (moe_route,
+ * moe_dispatch, moe_expert_ffn): the device status word, the router's
+ * latent buffer and the dispatch counters.  Pure host function. */
+int moe_scratch_size(const moe_dims* dims, size_t* bytes);
+
+/* Bytes of workspace needed by moe_forward: the scratch above plus every
+ * intermediate of the layer (routing results, permutation, x_perm, act,
+ * y_perm).  Any buffer of this size also serves every stage call. */
+int moe_workspace_size(const moe_dims* dims, size_t* bytes);
+
+/* Bytes of workspace needed by moe_forward_host: moe_workspace_size plus
+ * device staging for x and out. */
+int moe_workspace_size_host(const moe_dims* dims, size_t* bytes);
+
+/* Zeroes the sticky device status word in `ws` (enqueued on `stream`). */
+int moe_clear_device_status(void* ws, void* stream);
+
+/* Synchronises `stream`, then copies the device status word of `ws` to
+ * *status (host).  Returns MOE_OK if it is zero, MOE_ERR_DEVICE_STATUS if
+ * not (the word is left as is), MOE_ERR_CUDA if the sync failed. */
+int moe_get_device_status(void* ws, int32_t* status, void* stream);
+
+/* Builds the interleaved gate/up weight used by moe_expert_ffn:
+ *   w13[e] is [2*inter, d]; for block b = 0 .. inter/64 - 1 its rows
+ *   [128b, 128b+64) are w_gate[e][64b, 64b+64) and rows [128b+64, 128b+128)
+ *   are w_up[e][64b, 64b+64).
+ * w_gate, w_up: [E, inter, d] bf16.  w13: [E, 2*inter, d] bf16 (written). */
+int moe_prepare_weights(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up,
+                        moe_bf16* w13, void* stream);
+
+/* Routing (latent projection, summed head scores, softmax, top-k, gates).
+ *   x        [T, d] bf16
+ *   w_lat    [n_heads*head_dim, d] bf16
+ *   w_head   [E, n_heads*head_dim] bf16
+ *   bias     [E] fp32 or NULL (added to the summed scores before the softmax)
+ *   topk_idx [T, top_k] int32 (written): expert ids, slot order as above
+ *   topk_gate[T, top_k] fp32 (written): renormalised gates
+ *   logits   [T, E] fp32 or NULL: if given, the summed scores s (bias included)
+ *   ws       scratch of at least moe_scratch_size bytes
+ * The latent vector h is accumulated in fp32 on the tensor cores and fed to
+ * the head-score product as a bf16 hi + lo pair, so s carries fp32-level
+ * accuracy although both products run as bf16 tensor-core GEMMs. */
+int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+              const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Sorting: counting-sort permutation of the T*top_k (token, slot) pairs into
+ * expert-contiguous order, then the row gather.
+ *   topk_idx  [T, top_k] int32 (read)
+ *   offsets   [E + 1] int32 (written): exclusive prefix of per-expert counts
+ *   row_of    [T, top_k] int32 (written): destination row of (t, slot);
+ *             the row of (t, e) is offsets[e] + #{t' < t that chose e}
+ *   src_token [T*top_k] int32 (written): src_token[row_of[t, s]] = t
+ *   x_perm    [T*top_k, d] bf16 (written): x_perm[r] = x[src_token[r]]
+ * The result is deterministic.  An id outside [0, E) sets
+ * MOE_DEV_BAD_EXPERT_ID; that pair is left out of every output. */
+int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx, int32_t* offsets,
+                 int32_t* row_of, int32_t* src_token, moe_bf16* x_perm,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Calculation: grouped SwiGLU expert GEMMs over ragged expert groups.
+ *   x_perm  [T*top_k, d] bf16, rows of expert e are [offsets[e], offsets[e+1])
+ *   offsets [E + 1] int32 device array (read on the device only)
+ *   w13     [E, 2*inter, d] bf16 from moe_prepare_weights
+ *   w_down  [E, d, inter] bf16
+ *   act     [T*top_k, inter] bf16 (written; caller-owned intermediate):
+ *           silu(x W_gate^T) * (x W_up^T), fp32 accumulate, one bf16 rounding
+ *   y_perm  [T*top_k, d] bf16 (written): act W_down^T, fp32 accumulate
+ * y_perm may alias x_perm. */
+int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets,
+                   const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Gate-weighted combine, scatter-free (one writer per output row):
+ *   out[t] = sum_{s < top_k} topk_gate[t, s] * y_perm[row_of[t, s]]
+ * summed in slot order in fp32, rounded once to bf16.  A row index outside
+ * [0, T*top_k) contributes nothing.
+ *   y_perm [T*top_k, d] bf16, row_of [T, top_k] int32, topk_gate [T, top_k] fp32,
+ *   out [T, d] bf16 (written). */
+int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row_of,
+                const float* topk_gate, moe_bf16* out, void* stream);
+
+/* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, moe_combine on
+ * one stream, intermediates in `ws` (at least moe_workspace_size bytes).
+ * Clears the device status word first.  Weights: w13 from
+ * moe_prepare_weights, w_down [E, d, inter]. */
+int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward for a caller whose activations live in host memory: copies
+ * x_host [T, d] to the device, runs the layer, copies out to out_host [T, d]
+ * and synchronises `stream`.  Weights are device pointers.  Host buffers
+ * should be page-locked for full copy bandwidth.  ws: at least
+ * moe_workspace_size_host bytes. */
+int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* w_lat,
+                     const moe_bf16* w_head, const float* bias, const moe_bf16* w13,
+                     const moe_bf16* w_down, moe_bf16* out_host, void* ws, size_t ws_bytes,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,85 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and its host-side checks reject bad arguments before any CUDA call."""
+import ctypes
+
+import pytest
+
+import fine_grained_moe_02_b300 as moe
+from fine_grained_moe_02_b300 import binding as B
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fine_grained_moe_02_b300 import build
+    build.build()
+    return moe.lib()
+
+
+def test_every_header_function_is_exported(L):
+    names = moe.header_functions()
+    assert len(names) >= 14
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(names) == set(B._SIGS), "binding signatures out of sync with include/moe.h"
+
+
+def test_status_strings(L):
+    assert moe.status_string(0) == "MOE_OK"
+    assert moe.status_string(-4) == "MOE_ERR_WORKSPACE_TOO_SMALL"
+    assert moe.status_string(12345) == "MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("kw,ok", [
+    (dict(T=256, d=512, E=16, inter=128), True),
+    (dict(T=107520, d=4096, E=128, inter=1024), True),
+    (dict(T=48960, d=4096, E=256, inter=512), True),
+    (dict(T=1, d=64, E=8, inter=64, top_k=8), True),
+    (dict(T=0, d=512, E=16, inter=128), False),
+    (dict(T=256, d=500, E=16, inter=128), False),
+    (dict(T=256, d=512, E=16, inter=100), False),
+    (dict(T=256, d=512, E=257, inter=128), False),
+    (dict(T=256, d=512, E=4, inter=128, top_k=6), False),
+    (dict(T=256, d=512, E=16, inter=128, top_k=9), False),
+    (dict(T=256, d=512, E=16, inter=128, n_heads=12, head_dim=100), False),
+    (dict(T=400_000_000, d=512, E=16, inter=128), False),
+])
+def test_check_dims(L, kw, ok):
+    d = moe.moe_dims.make(**kw)
+    rc = moe.moe_check_dims(d)
+    assert (rc == 0) == ok, (kw, rc)
+    if not ok:
+        assert rc == B.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_workspace_sizes(L):
+    d = moe.moe_dims.make(107520, 4096, 128, 1024)
+    s, w, h = moe.moe_scratch_size(d), moe.moe_workspace_size(d), moe.moe_workspace_size_host(d)
+    Tk = 107520 * 6
+    assert s >= 107520 * 6144 * 2
+    assert w >= s + Tk * 4096 * 2 + Tk * 1024 * 2 + 4 * Tk * 4
+    assert h >= w + 2 * 107520 * 4096 * 2
+    with pytest.raises(moe.MoeError):
+        moe.moe_workspace_size(moe.moe_dims.make(0, 4096, 128, 1024))
+
+
+def test_null_and_misaligned_pointers_are_rejected_on_the_host(L):
+    d = moe.moe_dims.make(256, 512, 16, 128)
+    P = ctypes.c_void_p
+    ok, bad = P(0x10000), P(0x10001)
+    nul = None
+    # NULL required pointer
+    assert L.moe_route(ctypes.byref(d), nul, ok, ok, nul, ok, ok, nul, ok, 1 << 30, nul) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch(ctypes.byref(d), ok, nul, ok, ok, ok, ok, ok, 1 << 30, nul) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(d), ok, ok, nul, ok, nul) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_forward(ctypes.byref(d), ok, ok, ok, nul, ok, ok, ok, nul, 1 << 30, nul) == B.MOE_ERR_INVALID_ARG
+    # misaligned pointer
+    assert L.moe_route(ctypes.byref(d), bad, ok, ok, nul, ok, ok, nul, ok, 1 << 30, nul) == B.MOE_ERR_MISALIGNED
+    assert L.moe_expert_ffn(ctypes.byref(d), ok, ok, ok, ok, ok, bad, ok, 1 << 30, nul) == B.MOE_ERR_MISALIGNED
+    assert L.moe_combine(ctypes.byref(d), ok, ok, ok, bad, nul) == B.MOE_ERR_MISALIGNED
+    # workspace too small
+    assert L.moe_dispatch(ctypes.byref(d), ok, ok, ok, ok, ok, ok, ok, 64, nul) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_forward(ctypes.byref(d), ok, ok, ok, nul, ok, ok, ok, ok, 64, nul) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    # bad dims
+    d0 = moe.moe_dims.make(256, 500, 16, 128)
+    assert L.moe_route(ctypes.byref(d0), ok, ok, ok, nul, ok, ok, nul, ok, 1 << 30, nul) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_check_dims(None) == B.MOE_ERR_INVALID_ARG

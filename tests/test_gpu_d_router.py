@@ -1,0 +1,49 @@
+"""Router (two tcgen05 GEMMs with hi/lo latent split + fused top-k) vs oracle."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=256, d=512, E=16, inter=128),                               # the tiny workload's router
+    dict(T=1, d=512, E=16, inter=128),
+    dict(T=129, d=1024, E=64, inter=64, router_init="uniform"),
+    dict(T=300, d=256, E=256, inter=64, top_k=8),
+    dict(T=200, d=512, E=6, inter=64, top_k=6),                         # k == E: gates = full softmax
+    dict(T=333, d=768, E=40, inter=64, top_k=1),                        # E not a power of two
+    dict(T=130, d=128, E=128, inter=64, n_heads=2, head_dim=128),      # other head geometry
+])
+def test_router_matches_oracle(kw):
+    inp = G.small_inputs(**kw)
+    dev = G.Dev(inp)
+    idx, gate, logits = dev.route()
+    assert dev.status() == 0
+    s_ref = G.oracle_logits(inp)
+    stats = G.check_routing(s_ref, idx.cpu().numpy(), gate.cpu().numpy(), inp["cfg"].top_k,
+                            logits.cpu().numpy())
+    assert stats["near_ties"] <= max(3, inp["cfg"].T // 50)
+
+
+def test_router_bias_forces_experts():
+    inp = G.small_inputs(T=500, d=256, E=32, inter=64)
+    b = np.zeros(32, np.float32)
+    b[[3, 9, 12, 20, 27, 31]] = np.array([60, 50, 40, 30, 20, 10], np.float32)
+    inp["bias"] = b
+    dev = G.Dev(inp)
+    idx, gate, logits = dev.route()
+    got = idx.cpu().numpy()
+    assert np.all(got == np.array([3, 9, 12, 20, 27, 31]))
+    G.check_routing(G.oracle_logits(inp), got, gate.cpu().numpy(), 6, logits.cpu().numpy())
+
+
+def test_router_without_logits_output_gives_same_routing():
+    inp = G.small_inputs(T=700, d=512, E=64, inter=64)
+    dev = G.Dev(inp)
+    i1, g1, _ = dev.route(want_logits=True)
+    i2, g2, _ = dev.route(want_logits=False)
+    assert torch.equal(i1, i2) and torch.equal(g1, g2)
