@@ -32,7 +32,7 @@ def test_router_matches_oracle(kw):
 def test_router_bias_forces_experts():
     inp = G.small_inputs(T=500, d=256, E=32, inter=64)
     b = np.zeros(32, np.float32)
-    b[[3, 9, 12, 20, 27, 31]] = np.array([60, 50, 40, 30, 20, 10], np.float32)
+    b[[3, 9, 12, 20, 27, 31]] = np.array([600, 500, 400, 300, 200, 100], np.float32)
     inp["bias"] = b
     dev = G.Dev(inp)
     idx, gate, logits = dev.route()
