@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""MoE-layer forward throughput on B300 (tokens/s), with roofline fractions.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload clip] [--impl ours|reference]
+
+One step = one forward pass of the whole layer (routing, sorting, both expert
+GEMMs, combine) over one batch of synthetic tokens resident in HBM, run
+through libmoe's C ABI.  The default workload is the full 10 s preview clip
+(T=107520 tokens, d=4096, E=128 experts, inter=1024, top-6, 12x256 latent
+routing, Zipf(1.2)-skewed router bias).  For N > 1 (torchrun) every rank
+runs its own clip on its own GPU with no exchange (token sharding needs
+none): weak scaling, value = tokens over all ranks / max-over-ranks time.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on
+a bounded token sample per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from dataclasses import replace
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE-layer tokens/sec on 1 B300; grouped-GEMM % bf16 TC peak; permute GB/s"
+KERNELS_PER_STEP = 9  # 2 router GEMMs, 4 sorting kernels, 2 expert GEMMs, combine
+GEMM_SOURCES = ["gemm_tc.cuh", "epilogues.cuh", "ptx.cuh", "gemm_launch.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="clip", choices=mi.CONFIG_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=512, help="tokens in the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, world
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        j = json.loads(p.read_text())
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+
+
+def workload_str(cfg) -> str:
+    extra = {"zipf": f", Zipf({cfg.zipf_s}) router bias"}.get(cfg.bias, "")
+    if cfg.router_init == "uniform":
+        extra += ", uniform router init"
+    if cfg.modality_split:
+        extra += ", video|text|audio x scales " + "/".join(str(s) for _, s in cfg.modality_split)
+    return (f"{cfg.name}: T={cfg.T}, d={cfg.d}, E={cfg.E}, inter={cfg.inter}, top-{cfg.top_k}, "
+            f"{cfg.n_heads}x{cfg.head_dim} latent routing{extra}")
+
+
+def algorithmic(cfg) -> dict:
+    """Algorithmic flops and bytes per step (routed rows only, no tile padding)."""
+    T, d, E, I, k, L = cfg.T, cfg.d, cfg.E, cfg.inter, cfg.top_k, cfg.L
+    Tk = T * k
+    return dict(
+        router_flops=2 * T * d * L + 2 * T * (2 * L) * E,     # latent GEMM + hi/lo score GEMM
+        gemm1_flops=2 * Tk * d * 2 * I,
+        gemm2_flops=2 * Tk * I * d,
+        permute_bytes=T * d * 2 + Tk * d * 2,                 # read x once, write x_perm
+        combine_bytes=Tk * d * 2 + Tk * 8 + T * d * 2,        # read y rows + idx/gates, write out
+    )
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.f.flush()
+        rows = [ln.split(",") for ln in Path(self.f.name).read_text().splitlines() if ln.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons, pw = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+def gemm_src_hash() -> str:
+    h = hashlib.sha256()
+    for n in GEMM_SOURCES:
+        h.update((ROOT / "fine_grained_moe_02_b300" / "csrc" / n).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """Per-launch DRAM bytes of expert GEMM-1 from the committed ncu summary, if
+    the kernel sources still match the ones it was captured from."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None, "no ncu capture"
+    j = json.loads(p.read_text())
+    ent = j.get(workload)
+    if not ent:
+        return None, "no ncu capture for this workload"
+    if ent.get("src_hash") != gemm_src_hash():
+        return None, "kernel changed since the ncu capture"
+    return ent["dram_bytes_per_launch"], ent.get("note", "")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm
+# ---------------------------------------------------------------------------
+
+def oracle_step(inp, tokens, widened):
+    from oracle import moe_oracle as O
+    cfg = inp["cfg"]
+    x = O.widen_bf16(inp["x"][tokens])
+    if widened is not None:
+        return O.forward(x, widened["w_lat"], widened["w_head"], inp["bias"], widened["w_gate"],
+                         widened["w_up"], widened["w_down"], cfg.n_heads, cfg.head_dim, cfg.top_k)
+    return O.forward(x, O.widen_bf16(inp["w_lat"]), O.widen_bf16(inp["w_head"]), inp["bias"], inp["w_gate"],
+                     inp["w_up"], inp["w_down"], cfg.n_heads, cfg.head_dim, cfg.top_k,
+                     widen_experts=O.widen_bf16)
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except Exception:  # noqa: BLE001
+        return os.cpu_count()
+
+
+def cpu_baseline(inp, n_tokens: int) -> dict:
+    """The oracle as it stands on a bounded token sample (full weights)."""
+    cfg = inp["cfg"]
+    tokens = mi.sample_tokens(cfg.T, n_tokens, seed=7)
+    t0 = time.perf_counter()
+    oracle_step(inp, tokens, None)
+    dt = time.perf_counter() - t0
+    return {"value": len(tokens) / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{len(tokens)} seeded tokens of the {cfg.name} workload, full weights, one fp64 "
+                      f"forward incl. per-expert bf16->fp64 widening ({dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import psutil
+    from oracle import moe_oracle as O
+    cfg = mi.CONFIGS[args.workload]
+    inp = mi.make_inputs(cfg)
+    weight_bytes_f64 = 8 * (inp["w_gate"].size + inp["w_up"].size + inp["w_down"].size)
+    widened = None
+    if psutil.virtual_memory().available > 2.5 * weight_bytes_f64:
+        widened = {k: O.widen_bf16(inp[k]) for k in ("w_lat", "w_head", "w_gate", "w_up", "w_down")}
+    per_step = max(16, min(256, 4096 // max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        oracle_step(inp, mi.sample_tokens(cfg.T, per_step, seed=1000 + i), widened)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(inp, mi.sample_tokens(cfg.T, per_step, seed=i), widened)
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    sample = (f"{per_step} seeded tokens of the {cfg.name} workload per step, full weights"
+              + (" (pre-widened to fp64 once, untimed)" if widened is not None else ", widened per step"))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_str(cfg)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    rank, local, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import torch.distributed as dist
+    import fine_grained_moe_02_b300 as moe
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cfg = mi.CONFIGS[args.workload]
+    inp = mi.make_weights(cfg)
+    inp["x"] = mi.make_x(replace(cfg, seed=cfg.seed + rank))   # each rank its own tokens
+    inp["cfg"] = cfg
+    T, d, E, I, k = cfg.T, cfg.d, cfg.E, cfg.inter, cfg.top_k
+    dims = moe.moe_dims.make(T, d, E, I, k, cfg.n_heads, cfg.head_dim)
+
+    def up(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).cuda()
+
+    x = up(inp["x"])
+    w_lat, w_head, w_down = up(inp["w_lat"]), up(inp["w_head"]), up(inp["w_down"])
+    bias = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).cuda()
+    w13 = torch.empty((E, 2 * I, d), dtype=torch.bfloat16, device="cuda")
+    wg, wu = up(inp["w_gate"]), up(inp["w_up"])
+    moe.moe_prepare_weights(dims, wg, wu, w13)
+    del wg, wu
+    ws = moe.alloc_workspace(moe.moe_workspace_size(dims))
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    row_of = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    src = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device="cuda")
+    act = torch.empty((T * k, I), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        # exactly moe_forward's sequence, with an event between stages
+        moe.moe_clear_device_status(ws)
+        if ev: ev[0].record(stream)
+        moe.moe_route(dims, x, w_lat, w_head, bias, idx, gate, None, ws)
+        if ev: ev[1].record(stream)
+        moe.moe_dispatch(dims, x, idx, offsets, row_of, src, x_perm, ws)
+        if ev: ev[2].record(stream)
+        moe.moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws)
+        if ev: ev[3].record(stream)
+        moe.moe_expert_gemm2(dims, act, offsets, w_down, x_perm, ws)   # y_perm aliases x_perm
+        if ev: ev[4].record(stream)
+        moe.moe_combine(dims, x_perm, row_of, gate, out)
+        if ev: ev[5].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    status = moe.moe_get_device_status(ws)
+    if status != 0:
+        raise SystemExit(f"device status {status:#x} after warm-up")
+    counts = np.diff(offsets.cpu().numpy())
+
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    clocks = Clocks(vis[local] if local < len(vis) else local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.start()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    stage_names = ["route", "dispatch", "gemm1", "gemm2", "combine"]
+    stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(stage_names)}
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status set during the timed region")
+
+    # moe_forward itself (the same sequence in one C call), for the record
+    fwd_ms = None
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    a0.record(stream)
+    n_fwd = max(3, args.steps // 5)
+    for _ in range(n_fwd):
+        moe.moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws)
+    a1.record(stream)
+    barrier()
+    fwd_ms = a0.elapsed_time(a1) / n_fwd
+
+    # end to end through the public host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        ws_h = moe.alloc_workspace(moe.moe_workspace_size_host(dims))
+        xh = x.cpu().pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        for _ in range(2):
+            moe.moe_forward_host(dims, xh, w_lat, w_head, bias, w13, w_down, oh, ws_h)
+        n_e2e = max(3, args.steps // 5)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            moe.moe_forward_host(dims, xh, w_lat, w_head, bias, w13, w_down, oh, ws_h)
+        barrier()
+        dt = (time.perf_counter() - t0) / n_e2e
+        if world > 1:
+            tt = torch.tensor([dt], dtype=torch.float64, device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            dt = float(tt.item())
+        e2e = {"value": world * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": world * T * d * 2,
+               "d2h_bytes_per_step": world * T * d * 2, "ms_per_step": 1000 * dt,
+               "path": "moe_forward_host (pinned host x and out, copies + layer + stream sync per step)"}
+        del ws_h
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    alg = algorithmic(cfg)
+    ms_step = elapsed_ms / args.steps
+    value = world * T * args.steps / (elapsed_ms / 1e3)
+    g1_tf = alg["gemm1_flops"] / (stage_ms["gemm1"] * 1e-3) / 1e12
+    g2_tf = alg["gemm2_flops"] / (stage_ms["gemm2"] * 1e-3) / 1e12
+    gg_tf = (alg["gemm1_flops"] + alg["gemm2_flops"]) / ((stage_ms["gemm1"] + stage_ms["gemm2"]) * 1e-3) / 1e12
+    perm_gbs = alg["permute_bytes"] / (stage_ms["dispatch"] * 1e-3) / 1e9
+    comb_gbs = alg["combine_bytes"] / (stage_ms["combine"] * 1e-3) / 1e9
+    traffic, traffic_note = measured_traffic(cfg.name)
+    tag = "of measured" if pk["source"] == "measured" else "of fallback"
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_str(cfg), "tokens_per_step_per_gpu": T,
+                   "parallelism": f"token-sharded replicas x{world}, no collective",
+                   "l2": "no flush: inputs larger than L2 (x 0.88 GB, expert weights 3.2 GB > 126 MB)"
+                   if cfg.name == "clip" else "no flush",
+                   "expert_rows_min_max": [int(counts.min()), int(counts.max())]},
+        "stages_ms": stage_ms,
+        "forward_call_ms": fwd_ms,
+        "grouped_gemm_tflops": gg_tf,
+        "grouped_gemm_frac_bf16_peak": gg_tf / pk["bf16_sus"],
+        "gemm1_tflops": g1_tf, "gemm2_tflops": g2_tf,
+        "router_tflops": alg["router_flops"] / (stage_ms["route"] * 1e-3) / 1e12,
+        "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm"],
+        "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm"],
+        "roofline": {"kernel": "expert GEMM-1 + SwiGLU (gemm_tc_kernel<256, EpiSwiGLU>)", "bound": "tensor",
+                     "achieved": g1_tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": g1_tf / pk["bf16_sus"],
+                     "peak_kind": f"bf16 dense sustained ({tag}; kernel timed inside a long step)",
+                     "traffic": traffic, "traffic_note": traffic_note,
+                     "algorithmic_flops_per_launch": alg["gemm1_flops"]},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, args.cpu_sample)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

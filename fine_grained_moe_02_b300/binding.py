@@ -64,6 +64,8 @@ _SIGS = {
     "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_expert_gemm1": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_expert_gemm2": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P]),
     "moe_forward": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_host": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -194,6 +196,20 @@ def moe_expert_ffn(dims, x_perm, offsets, w13, w_down, act, y_perm, ws, stream=N
     _dev(offsets, dtype=torch.int32)
     _check(lib().moe_expert_ffn(ctypes.byref(dims), _ptr(x_perm), _ptr(offsets), _ptr(w13), _ptr(w_down),
                                 _ptr(act), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws, stream=None) -> None:
+    _dev(x_perm, w13, act, dtype=torch.bfloat16)
+    _dev(offsets, dtype=torch.int32)
+    _check(lib().moe_expert_gemm1(ctypes.byref(dims), _ptr(x_perm), _ptr(offsets), _ptr(w13), _ptr(act),
+                                  _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_gemm1")
+
+
+def moe_expert_gemm2(dims, act, offsets, w_down, y_perm, ws, stream=None) -> None:
+    _dev(act, w_down, y_perm, dtype=torch.bfloat16)
+    _dev(offsets, dtype=torch.int32)
+    _check(lib().moe_expert_gemm2(ctypes.byref(dims), _ptr(act), _ptr(offsets), _ptr(w_down), _ptr(y_perm),
+                                  _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_gemm2")
 
 
 def moe_combine(dims, y_perm, row_of, topk_gate, out, stream=None) -> None:

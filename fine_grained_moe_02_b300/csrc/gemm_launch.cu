@@ -106,29 +106,30 @@ int launch_route(const RouteArgs& a, cudaStream_t stream) {
   }
 }
 
-// Expert GEMMs over ragged groups (device offsets): GEMM-1 + SwiGLU, GEMM-2.
-int launch_ffn(const FfnArgs& a, cudaStream_t stream) {
+// Expert GEMM-1 over ragged groups (device offsets), SwiGLU fused: act = silu(x Wg^T) * (x Wu^T).
+int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb;
   const int rows = static_cast<int>(a.rows);
-  {
-    const int n = 2 * a.I;
-    const int bn = (n % 256 == 0) ? 256 : 128;
-    if (!make_tmap_bf16_2d(&ta, a.x_perm, a.d, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
-    GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status};
-    EpiSwiGLU::Params ep{a.act, a.I};
-    const int rc = (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream)
-                               : run_gemm<128, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream);
-    if (rc != MOE_OK) return rc;
-  }
-  {
-    const int bn = pick_bn(a.d);
-    if (!make_tmap_bf16_2d(&ta, a.act, a.I, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, bn)) return MOE_ERR_CUDA;
-    GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
-    EpiStoreBf16::Params ep{a.y_perm, a.d};
-    return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, sh, ep, a.sm_count, stream);
-  }
+  const int n = 2 * a.I;
+  const int bn = (n % 256 == 0) ? 256 : 128;
+  if (!make_tmap_bf16_2d(&ta, a.x_perm, a.d, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
+  GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status};
+  EpiSwiGLU::Params ep{a.act, a.I};
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream)
+                     : run_gemm<128, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream);
+}
+
+// Expert GEMM-2 over ragged groups: y_perm = act Wd^T.
+int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  const int rows = static_cast<int>(a.rows);
+  const int bn = pick_bn(a.d);
+  if (!make_tmap_bf16_2d(&ta, a.act, a.I, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, bn)) return MOE_ERR_CUDA;
+  GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
+  EpiStoreBf16::Params ep{a.y_perm, a.d};
+  return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, sh, ep, a.sm_count, stream);
 }
 
 // w13[e, 128b + j] = j < 64 ? w_gate[e, 64b + j] : w_up[e, 64b + j - 64]   (rows of d)

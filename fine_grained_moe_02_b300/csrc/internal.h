@@ -66,7 +66,8 @@ struct CombineArgs {
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 size_t dispatch_scratch_bytes(int64_t T, int E);
 int launch_route(const RouteArgs& a, cudaStream_t stream);
-int launch_ffn(const FfnArgs& a, cudaStream_t stream);
+int launch_gemm1(const FfnArgs& a, cudaStream_t stream);
+int launch_gemm2(const FfnArgs& a, cudaStream_t stream);
 int launch_combine(const CombineArgs& a, cudaStream_t stream);
 int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w13, int E, int I, int d,
                        cudaStream_t stream);

@@ -226,9 +226,64 @@ int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_id
   return launch_dispatch(a, static_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared checks of the expert-GEMM entry points; fills `a` on success.
+int ffn_args(const moe_dims* dims, const int32_t* offsets, void* ws, size_t ws_bytes, FfnArgs& a) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (offsets == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(offsets) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < scratch_layout(dims).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  a = FfnArgs{};
+  a.offsets = offsets;
+  a.rows = dims->T * dims->top_k;
+  a.d = dims->d;
+  a.I = dims->inter;
+  a.E = dims->E;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets, const moe_bf16* w13,
+                     moe_bf16* act, void* ws, size_t ws_bytes, void* stream) {
+  FfnArgs a;
+  int rc = ffn_args(dims, offsets, ws, ws_bytes, a);
+  if (rc != MOE_OK) return rc;
+  if (x_perm == nullptr || w13 == nullptr || act == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w13) || !aligned16(act)) return MOE_ERR_MISALIGNED;
+  a.x_perm = x_perm;
+  a.w13 = w13;
+  a.act = act;
+  return launch_gemm1(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_gemm2(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets, const moe_bf16* w_down,
+                     moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  FfnArgs a;
+  int rc = ffn_args(dims, offsets, ws, ws_bytes, a);
+  if (rc != MOE_OK) return rc;
+  if (act == nullptr || w_down == nullptr || y_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(act) || !aligned16(w_down) || !aligned16(y_perm)) return MOE_ERR_MISALIGNED;
+  a.act = const_cast<moe_bf16*>(act);  // read only (TMA source)
+  a.w_down = w_down;
+  a.y_perm = y_perm;
+  return launch_gemm2(a, static_cast<cudaStream_t>(stream));
+}
+
 int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets, const moe_bf16* w13,
                    const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm, void* ws, size_t ws_bytes,
                    void* stream) {
+  // all checks before the first launch, so a bad argument launches nothing
   int rc = moe_check_dims(dims);
   if (rc != MOE_OK) return rc;
   if (x_perm == nullptr || offsets == nullptr || w13 == nullptr || w_down == nullptr || act == nullptr ||
@@ -238,22 +293,9 @@ int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* 
       !aligned16(y_perm) || !aligned16(ws))
     return MOE_ERR_MISALIGNED;
   if (ws_bytes < scratch_layout(dims).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  const int sms = sm_count_current();
-  if (sms <= 0) return MOE_ERR_CUDA;
-  FfnArgs a{};
-  a.x_perm = x_perm;
-  a.offsets = offsets;
-  a.w13 = w13;
-  a.w_down = w_down;
-  a.act = act;
-  a.y_perm = y_perm;
-  a.rows = dims->T * dims->top_k;
-  a.d = dims->d;
-  a.I = dims->inter;
-  a.E = dims->E;
-  a.status = status_ptr(ws);
-  a.sm_count = sms;
-  return launch_ffn(a, static_cast<cudaStream_t>(stream));
+  rc = moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws, ws_bytes, stream);
+  if (rc != MOE_OK) return rc;
+  return moe_expert_gemm2(dims, act, offsets, w_down, y_perm, ws, ws_bytes, stream);
 }
 
 int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row_of, const float* topk_gate,
@@ -285,7 +327,9 @@ int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, 
   if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
       out == nullptr || ws == nullptr)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(w13) || !aligned16(w_down) ||
+      !aligned16(out) || !aligned16(ws) || (bias != nullptr && !aligned16(bias)))
+    return MOE_ERR_MISALIGNED;
   const ForwardLayout f = forward_layout(dims);
   if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;

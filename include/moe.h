@@ -163,6 +163,15 @@ int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* 
                    const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* The two halves of moe_expert_ffn, for callers that schedule or time them
+ * separately.  moe_expert_gemm1 writes act = silu(x W_gate^T) * (x W_up^T);
+ * moe_expert_gemm2 writes y_perm = act W_down^T.  Arguments as in
+ * moe_expert_ffn. */
+int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets, const moe_bf16* w13,
+                     moe_bf16* act, void* ws, size_t ws_bytes, void* stream);
+int moe_expert_gemm2(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets, const moe_bf16* w_down,
+                     moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream);
+
 /* Gate-weighted combine, scatter-free (one writer per output row):
  *   out[t] = sum_{s < top_k} topk_gate[t, s] * y_perm[row_of[t, s]]
  * summed in slot order in fp32, rounded once to bf16.  A row index outside
