@@ -61,6 +61,28 @@ def dist_env():
     return rank, local, world
 
 
+def rank_workload(cfg, rank: int):
+    """Token sharding: rank r runs its own batch of the workload (seed + r for
+    x, shared weights), so per-GPU work is fixed as N grows."""
+    return replace(cfg, seed=cfg.seed + rank)
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(tokens_per_rank: int, world: int, steps: int, max_elapsed_s: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / max_elapsed_s
+
+
 def peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -253,7 +275,7 @@ def main():
 
     cfg = mi.CONFIGS[args.workload]
     inp = mi.make_weights(cfg)
-    inp["x"] = mi.make_x(replace(cfg, seed=cfg.seed + rank))   # each rank its own tokens
+    inp["x"] = mi.make_x(rank_workload(cfg, rank))   # each rank its own tokens
     inp["cfg"] = cfg
     T, d, E, I, k = cfg.T, cfg.d, cfg.E, cfg.inter, cfg.top_k
     dims = moe.moe_dims.make(T, d, E, I, k, cfg.n_heads, cfg.head_dim)
@@ -319,11 +341,7 @@ def main():
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
     stage_names = ["route", "dispatch", "gemm1", "gemm2", "combine"]
     stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(stage_names)}
     if moe.moe_get_device_status(ws) != 0:
@@ -355,11 +373,7 @@ def main():
         for _ in range(n_e2e):
             moe.moe_forward_host(dims, xh, w_lat, w_head, bias, w13, w_down, oh, ws_h)
         barrier()
-        dt = (time.perf_counter() - t0) / n_e2e
-        if world > 1:
-            tt = torch.tensor([dt], dtype=torch.float64, device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            dt = float(tt.item())
+        dt = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, "cuda")
         e2e = {"value": world * T / dt, "unit": "tokens/s", "h2d_bytes_per_step": world * T * d * 2,
                "d2h_bytes_per_step": world * T * d * 2, "ms_per_step": 1000 * dt,
                "path": "moe_forward_host (pinned host x and out, copies + layer + stream sync per step)"}
@@ -373,7 +387,7 @@ def main():
     pk = peaks()
     alg = algorithmic(cfg)
     ms_step = elapsed_ms / args.steps
-    value = world * T * args.steps / (elapsed_ms / 1e3)
+    value = throughput(T, world, args.steps, elapsed_ms / 1e3)
     g1_tf = alg["gemm1_flops"] / (stage_ms["gemm1"] * 1e-3) / 1e12
     g2_tf = alg["gemm2_flops"] / (stage_ms["gemm2"] * 1e-3) / 1e12
     gg_tf = (alg["gemm1_flops"] + alg["gemm2_flops"]) / ((stage_ms["gemm1"] + stage_ms["gemm2"]) * 1e-3) / 1e12

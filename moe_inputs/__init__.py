@@ -74,8 +74,12 @@ CONFIGS = {
                       note="full 10 s preview clip: 60 latent frames x 1792 tokens, Zipf(1.2) router bias"),
     "refiner": MoeConfig("refiner", T=48960, d=4096, E=256, inter=512, router_init="uniform",
                          note="refiner chunk: 6 latent frames x 68x120 tokens, E=256, inter=512, uniform routing"),
+    # not one of the pages' workloads: a 4096-token slice at clip width with 32
+    # experts, small enough (~1.5 GB on the device) for full profiler captures
+    "slice": MoeConfig("slice", T=4096, d=4096, E=32, inter=1024,
+                       note="profiling size: 4096 tokens, d=4096, E=32, inter=1024"),
 }
-CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner"]
+CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "slice"]
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
