@@ -63,6 +63,7 @@ _SIGS = {
     "moe_prepare_weights": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_gemm1": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_gemm2": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -189,6 +190,15 @@ def moe_dispatch(dims, x, topk_idx, offsets, row_of, src_token, x_perm, ws, stre
     _dev(topk_idx, offsets, row_of, src_token, dtype=torch.int32)
     _check(lib().moe_dispatch(ctypes.byref(dims), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
                               _ptr(src_token), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(dims, x, topk_idx, offsets, row_of, src_token, x_perm, status=None, stream=None) -> None:
+    """moe_dispatch without a workspace (scratch in a fixed array inside libmoe)."""
+    _dev(x, x_perm, dtype=torch.bfloat16)
+    _dev(topk_idx, offsets, row_of, src_token, status, dtype=torch.int32)
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(dims), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
+                                      _ptr(src_token), _ptr(x_perm), _ptr(status), _stream(stream)),
+           "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(dims, x_perm, offsets, w13, w_down, act, y_perm, ws, stream=None) -> None:

@@ -1,0 +1,87 @@
+// moe_dispatch_noalloc: the sorting stage (histogram, scan, rank assignment,
+// row gather) for callers that cannot allocate device memory.  Its scratch is
+// a fixed array in the library's own device image instead of a caller
+// workspace; see include/moe.h for the contract.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "moe.h"
+
+namespace {
+
+// Per-block expert counters and bases, ceil(T / 2048) * E cells each.
+constexpr int64_t kNoAllocMaxCells = 65536;
+constexpr int64_t kSinkInts = 64;  // status sink when the caller passes no status word
+
+// Lives for as long as the library is loaded, on every GPU that loads it.
+static __device__ __align__(256) int32_t g_dispatch_scratch[kSinkInts + 2 * kNoAllocMaxCells];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int32_t* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_dispatch_scratch on the current device.  Host code may
+// not use the symbol itself (on the host it names a stand-in, not device
+// memory), so the address is looked up once per device and cached.
+int scratch_address(int32_t** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int moe_dispatch_noalloc(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx,
+                                    int32_t* offsets, int32_t* row_of, int32_t* src_token, moe_bf16* x_perm,
+                                    int32_t* status, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || topk_idx == nullptr || offsets == nullptr || row_of == nullptr || src_token == nullptr ||
+      x_perm == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(offsets) || !aligned16(row_of) ||
+      !aligned16(src_token) || !aligned16(x_perm) || (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u)))
+    return MOE_ERR_MISALIGNED;
+  // the counters need ceil(T / 2048) * E cells of each kind
+  const int64_t cells = static_cast<int64_t>(moe::dispatch_scratch_bytes(dims->T, dims->E) / (2 * sizeof(int32_t)));
+  if (cells > kNoAllocMaxCells) return MOE_ERR_UNSUPPORTED_SHAPE;
+
+  int32_t* scratch = nullptr;
+  if ((rc = scratch_address(&scratch)) != MOE_OK) return rc;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return MOE_ERR_CUDA;
+
+  // Every cell the kernels read is written earlier in the same call (the
+  // histogram pass writes all counters, the scan writes all bases), so
+  // nothing is cleared; the sink word is written but never read.
+  moe::DispatchArgs a{};
+  a.x = x;
+  a.topk_idx = topk_idx;
+  a.T = dims->T;
+  a.d = dims->d;
+  a.k = dims->top_k;
+  a.E = dims->E;
+  a.offsets = offsets;
+  a.row_of = row_of;
+  a.src_token = src_token;
+  a.x_perm = x_perm;
+  a.block_counts = scratch + kSinkInts;
+  a.block_base = scratch + kSinkInts + kNoAllocMaxCells;
+  a.status = status != nullptr ? status : scratch;
+  a.sm_count = sms;
+  return moe::launch_dispatch(a, static_cast<cudaStream_t>(stream));
+}

@@ -163,6 +163,32 @@ int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* 
                    const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* moe_dispatch for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point.
+ *
+ * Some callers cannot call cudaMalloc or hand over a workspace: code that
+ * runs inside a host framework which owns every byte of device memory and
+ * forbids allocation while work is being enqueued (plugin interfaces of
+ * inference runtimes), or latency-critical loops where an allocation's
+ * implicit device synchronisation is not acceptable.  This variant takes no
+ * workspace and allocates nothing: its counters live in a fixed array inside
+ * libmoe's device image, 64 + 2 * 65536 int32 (about 512 KiB), which every
+ * GPU that loads the library holds until the process exits.
+ *   - Arguments and results as in moe_dispatch (same kernels, same output).
+ *   - status: optional device int32 that receives MOE_DEV_* bits (OR-ed in;
+ *     the caller clears it).  NULL: device-detected problems are not reported.
+ *   - Limit: ceil(T / 2048) * E <= 65536 (e.g. T <= 1,048,576 at E = 128);
+ *     larger problems return MOE_ERR_UNSUPPORTED_SHAPE and launch nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents.  Every counter is rewritten before it is read, so nothing
+ *     needs clearing, but calls that overlap on the GPU (different streams,
+ *     or host threads enqueueing concurrently) race on it: serialise them. */
+int moe_dispatch_noalloc(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx, int32_t* offsets,
+                         int32_t* row_of, int32_t* src_token, moe_bf16* x_perm, int32_t* status, void* stream);
+
 /* The two halves of moe_expert_ffn, for callers that schedule or time them
  * separately.  moe_expert_gemm1 writes act = silu(x W_gate^T) * (x W_up^T);
  * moe_expert_gemm2 writes y_perm = act W_down^T.  Arguments as in
