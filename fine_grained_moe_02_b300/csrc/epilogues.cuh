@@ -1,5 +1,10 @@
 // Epilogues of the tcgen05 GEMM engine.  Each thread owns one accumulator
-// row (its TMEM lane) and walks the tile's columns 16 at a time.
+// row (its TMEM lane); a warp owns 32 consecutive rows of the tile.  Results
+// leave through a per-warp 32-row x 64-column staging chunk in shared memory
+// (128-byte swizzled, the layout the output tensor map uses) and one TMA bulk
+// store, so HBM sees whole 128-byte lines.  A warp whose 32 rows are cut by
+// the end of an expert group stores its valid rows with plain 16-byte stores
+// instead (the rows after the cut belong to the next group's tile).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -16,14 +21,53 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float (&v)[16]) {
-  uint4 a, b;
-  a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
-  a.z = pack_bf16x2(v[4], v[5]);   a.w = pack_bf16x2(v[6], v[7]);
-  b.x = pack_bf16x2(v[8], v[9]);   b.y = pack_bf16x2(v[10], v[11]);
-  b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
-  reinterpret_cast<uint4*>(dst)[0] = a;
-  reinterpret_cast<uint4*>(dst)[1] = b;
+// Loads 32 consecutive accumulator columns of this thread's row (one wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t a[16], b[16];
+  ptx::tmem_ld16(taddr, a);
+  ptx::tmem_ld16(taddr + 16, b);
+  ptx::tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = __uint_as_float(a[i]);
+    v[16 + i] = __uint_as_float(b[i]);
+  }
+}
+
+// Writes this warp's 32 rows x 64 bf16 columns (p[j] = columns 2j, 2j+1 of
+// this thread's row) to the output at (row0w, col0).  nvalid = rows of the 32
+// that may be written; row_ptr = this thread's row at col0 (fallback path).
+__device__ __forceinline__ void store_rows64(EpiCtx& ctx, int row0w, int col0, int nvalid, const uint32_t (&p)[32],
+                                             uint16_t* row_ptr) {
+  if (nvalid >= 32) {
+    if (ctx.pending) {  // the previous bulk store must be done reading the chunk
+      if (ctx.lane == 0) ptx::bulk_wait_read_all();
+      __syncwarp();
+    }
+    const uint32_t row_base = ctx.stage + static_cast<uint32_t>(ctx.lane) * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+      ptx::st_shared_v4(row_base + ((static_cast<uint32_t>(c) ^ (ctx.lane & 7u)) << 4), v);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (ctx.lane == 0) {
+      ptx::tma_store_2d(ctx.tmap, ctx.stage, col0, row0w);
+      ptx::bulk_commit();
+    }
+    ctx.pending = true;
+  } else if (ctx.lane < nvalid) {
+    uint4* dst = reinterpret_cast<uint4*>(row_ptr);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) dst[c] = make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+  }
+}
+
+__device__ __forceinline__ int warp_valid_rows(const TileCoord& c, const EpiCtx& ctx) {
+  const int first = c.row0 + ctx.quad * 32;
+  const int n = c.row_end - first;
+  return n < 0 ? 0 : (n > 32 ? 32 : n);
 }
 
 // out[row, n_blk*BN + j] = bf16(acc[j])  (expert GEMM-2: y_perm)
@@ -33,22 +77,24 @@ struct EpiStoreBf16 {
     int64_t ld;
   };
   template <int BN>
-  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r, int) {
+  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx& ctx) {
+    const int nvalid = warp_valid_rows(c, ctx);
     const int row = c.row0 + r;
-    const bool valid = row < c.row_end;
-    uint16_t* dst = p.out + static_cast<int64_t>(row) * p.ld + c.n_blk * BN;
-#pragma unroll 4
-    for (int col = 0; col < BN; col += 16) {
-      uint32_t u[16];
+    uint16_t* row_ptr = p.out + static_cast<int64_t>(row) * p.ld + c.n_blk * BN;
+#pragma unroll 1
+    for (int col = 0; col < BN; col += 64) {
+      uint32_t pk[32];
+      float v[32];
       __syncwarp();
-      ptx::tmem_ld16(taddr + col, u);
-      ptx::tmem_ld_wait();
-      if (valid) {
-        float v[16];
+      tmem_ld32(taddr + col, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(u[j]);
-        store16_bf16(dst + col, v);
-      }
+      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+      __syncwarp();
+      tmem_ld32(taddr + col + 32, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+      if (nvalid > 0) store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * BN + col, nvalid, pk, row_ptr + col);
     }
   }
 };
@@ -62,31 +108,30 @@ struct EpiSwiGLU {
     int64_t ld;
   };
   template <int BN>
-  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r, int) {
+  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx& ctx) {
     static_assert(BN % 128 == 0, "SwiGLU tiles hold whole 64+64 gate/up blocks");
+    const int nvalid = warp_valid_rows(c, ctx);
     const int row = c.row0 + r;
-    const bool valid = row < c.row_end;
-    uint16_t* dst = p.act + static_cast<int64_t>(row) * p.ld + c.n_blk * (BN / 2);
+    uint16_t* row_ptr = p.act + static_cast<int64_t>(row) * p.ld + c.n_blk * (BN / 2);
 #pragma unroll 1
     for (int j = 0; j < BN / 128; ++j) {
+      uint32_t pk[32];
 #pragma unroll
-      for (int cc = 0; cc < 64; cc += 16) {
-        uint32_t g[16], u[16];
+      for (int h = 0; h < 2; ++h) {
+        float g[32], u[32];
         __syncwarp();
-        ptx::tmem_ld16(taddr + j * 128 + cc, g);
-        ptx::tmem_ld16(taddr + j * 128 + 64 + cc, u);
-        ptx::tmem_ld_wait();
-        if (valid) {
-          float v[16];
+        tmem_ld32(taddr + j * 128 + h * 32, g);
+        tmem_ld32(taddr + j * 128 + 64 + h * 32, u);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float gv = __uint_as_float(g[i]);
-            const float uv = __uint_as_float(u[i]);
-            v[i] = gv / (1.0f + __expf(-gv)) * uv;
-          }
-          store16_bf16(dst + j * 64 + cc, v);
+        for (int i = 0; i < 16; ++i) {
+          const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
+          const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+          pk[h * 16 + i] = pack_bf16x2(a0, a1);
         }
       }
+      if (nvalid > 0)
+        store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * (BN / 2) + j * 64, nvalid, pk, row_ptr + j * 64);
     }
   }
 };
@@ -100,27 +145,32 @@ struct EpiHiLo {
     int L;
   };
   template <int BN>
-  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r, int) {
+  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx& ctx) {
+    const int nvalid = warp_valid_rows(c, ctx);
     const int row = c.row0 + r;
-    const bool valid = row < c.row_end;
-    uint16_t* dst = p.hl + static_cast<int64_t>(row) * p.ld + c.n_blk * BN;
-#pragma unroll 2
-    for (int col = 0; col < BN; col += 16) {
-      uint32_t u[16];
-      __syncwarp();
-      ptx::tmem_ld16(taddr + col, u);
-      ptx::tmem_ld_wait();
-      if (valid) {
-        float hi[16], lo[16];
+    uint16_t* row_ptr = p.hl + static_cast<int64_t>(row) * p.ld + c.n_blk * BN;
+#pragma unroll 1
+    for (int col = 0; col < BN; col += 64) {
+      uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float h = __uint_as_float(u[j]);
-          const float hb = __bfloat162float(__float2bfloat16_rn(h));
-          hi[j] = hb;
-          lo[j] = h - hb;  // exact in fp32; rounded to bf16 by the store
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        __syncwarp();
+        tmem_ld32(taddr + col + h * 32, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float h0 = v[2 * i], h1 = v[2 * i + 1];
+          const float b0 = __bfloat162float(__float2bfloat16_rn(h0));
+          const float b1 = __bfloat162float(__float2bfloat16_rn(h1));
+          hi[h * 16 + i] = pack_bf16x2(b0, b1);
+          lo[h * 16 + i] = pack_bf16x2(h0 - b0, h1 - b1);  // differences exact in fp32
         }
-        store16_bf16(dst + col, hi);
-        store16_bf16(dst + p.L + col, lo);
+      }
+      if (nvalid > 0) {
+        const int r0 = c.row0 + ctx.quad * 32, c0 = c.n_blk * BN + col;
+        store_rows64(ctx, r0, c0, nvalid, hi, row_ptr + col);
+        store_rows64(ctx, r0, p.L + c0, nvalid, lo, row_ptr + p.L + col);
       }
     }
   }
@@ -139,7 +189,8 @@ struct EpiTopK {
     int k;
   };
   template <int BN>
-  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r, int) {
+  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx&) {
     const int row = c.row0 + r;
     const bool valid = row < c.row_end;
     float bv[kMaxTopK];

@@ -32,26 +32,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 template <int BN, class Epi>
-int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& shape, const typename Epi::Params& ep,
-             int grid, cudaStream_t stream) {
+int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmShape& shape,
+             const typename Epi::Params& ep, int grid, cudaStream_t stream) {
   using S = GemmSmem<BN>;
   auto kern = gemm_tc_kernel<BN, Epi>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (grid < 1) grid = 1;
-  kern<<<grid, kGemmThreads, S::kDynBytes, stream>>>(ta, tb, shape, ep);
+  kern<<<grid, kGemmThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <class Epi>
-int run_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmShape& shape,
-                const typename Epi::Params& ep, int grid, cudaStream_t stream) {
+int run_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                const GemmShape& shape, const typename Epi::Params& ep, int grid, cudaStream_t stream) {
   switch (bn) {
-    case 256: return run_gemm<256, Epi>(ta, tb, shape, ep, grid, stream);
-    case 128: return run_gemm<128, Epi>(ta, tb, shape, ep, grid, stream);
-    case 64: return run_gemm<64, Epi>(ta, tb, shape, ep, grid, stream);
-    case 32: return run_gemm<32, Epi>(ta, tb, shape, ep, grid, stream);
-    case 16: return run_gemm<16, Epi>(ta, tb, shape, ep, grid, stream);
+    case 256: return run_gemm<256, Epi>(ta, tb, td, shape, ep, grid, stream);
+    case 128: return run_gemm<128, Epi>(ta, tb, td, shape, ep, grid, stream);
+    case 64: return run_gemm<64, Epi>(ta, tb, td, shape, ep, grid, stream);
+    case 32: return run_gemm<32, Epi>(ta, tb, td, shape, ep, grid, stream);
+    case 16: return run_gemm<16, Epi>(ta, tb, td, shape, ep, grid, stream);
     default: return MOE_ERR_UNSUPPORTED_SHAPE;
   }
 }
@@ -83,16 +83,17 @@ bool make_tmap_bf16_2d(void* tmap, const void* base, uint64_t cols, uint64_t row
 //         stage 2  s  = hl [W_head | W_head]^T + bias   dense GEMM, K = 2L, N = E, fused top-k
 int launch_route(const RouteArgs& a, cudaStream_t stream) {
   const int64_t m_tiles = (a.T + kBM - 1) / kBM;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, td;
   {
     const int bn = pick_bn(a.L);
     if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, kBM)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16_2d(&tb, a.w_lat, a.d, a.L, kBK, bn)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&td, a.hl, 2ULL * a.L, a.T, kBK, 32)) return MOE_ERR_CUDA;
     GemmShape sh{a.d, a.d, a.L, 1, nullptr, static_cast<int>(a.T), a.status};
     EpiHiLo::Params ep{a.hl, 2LL * a.L, a.L};
     const int64_t tiles = m_tiles * (a.L / bn);
     const int grid = static_cast<int>(tiles < a.sm_count ? tiles : a.sm_count);
-    const int rc = run_gemm_bn<EpiHiLo>(bn, ta, tb, sh, ep, grid, stream);
+    const int rc = run_gemm_bn<EpiHiLo>(bn, ta, tb, td, sh, ep, grid, stream);
     if (rc != MOE_OK) return rc;
   }
   {
@@ -102,34 +103,36 @@ int launch_route(const RouteArgs& a, cudaStream_t stream) {
     GemmShape sh{2 * a.L, a.L, bn, 1, nullptr, static_cast<int>(a.T), a.status};
     EpiTopK::Params ep{a.bias, a.logits, a.topk_idx, a.topk_gate, a.E, a.k};
     const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
-    return run_gemm_bn<EpiTopK>(bn, ta, tb, sh, ep, grid, stream);
+    return run_gemm_bn<EpiTopK>(bn, ta, tb, ta /* no bulk output */, sh, ep, grid, stream);
   }
 }
 
 // Expert GEMM-1 over ragged groups (device offsets), SwiGLU fused: act = silu(x Wg^T) * (x Wu^T).
 int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, td;
   const int rows = static_cast<int>(a.rows);
   const int n = 2 * a.I;
   const int bn = (n % 256 == 0) ? 256 : 128;
   if (!make_tmap_bf16_2d(&ta, a.x_perm, a.d, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&td, a.act, a.I, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status};
   EpiSwiGLU::Params ep{a.act, a.I};
-  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream)
-                     : run_gemm<128, EpiSwiGLU>(ta, tb, sh, ep, a.sm_count, stream);
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream)
+                     : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream);
 }
 
 // Expert GEMM-2 over ragged groups: y_perm = act Wd^T.
 int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, td;
   const int rows = static_cast<int>(a.rows);
   const int bn = pick_bn(a.d);
   if (!make_tmap_bf16_2d(&ta, a.act, a.I, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, bn)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&td, a.y_perm, a.d, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
   EpiStoreBf16::Params ep{a.y_perm, a.d};
-  return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, sh, ep, a.sm_count, stream);
+  return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream);
 }
 
 // w13[e, 128b + j] = j < 64 ? w_gate[e, 64b + j] : w_up[e, 64b + j - 64]   (rows of d)

@@ -35,6 +35,7 @@ constexpr int kUK = 16;           // k per tcgen05.mma (kind::f16)
 constexpr int kMaxGroups = 256;
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kOutChunkBytes = 32 * 128;          // 32 rows x 64 bf16
 
 struct GemmShape {
   int K;            // reduction length (A's columns)
@@ -55,8 +56,20 @@ struct GemmSmem {
   static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
   static constexpr int kAccStride = kTmemCols / 2;  // column offset of accumulator buffer 1
-  // ring + 1 KB slack for the manual 1024-byte alignment
-  static constexpr int kDynBytes = kStages * kStageBytes + 1024;
+  // one 32-row x 64-column bf16 staging chunk (4 KB, 128-byte swizzled) per epilogue warp
+  static constexpr int kOutBytes = 4 * kOutChunkBytes;
+  // ring + output staging + 1 KB slack for the manual 1024-byte alignment
+  static constexpr int kDynBytes = kStages * kStageBytes + kOutBytes + 1024;
+};
+
+// What an epilogue needs besides the accumulator: the output tensor map, this
+// warp's staging buffer and whether a bulk store from it may still be reading.
+struct EpiCtx {
+  const CUtensorMap* tmap;
+  uint32_t stage;   // shared address of this warp's 4 KB staging chunk
+  int lane;
+  int quad;         // TMEM lane quadrant = rows [32*quad, 32*quad + 32) of the tile
+  bool pending;     // lane 0 has a committed bulk store that may still read `stage`
 };
 
 struct TileCoord {
@@ -87,12 +100,12 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, con
 // Epi must provide:
 //   struct Params;
 //   template <int BN> static __device__ void run(const Params&, const TileCoord&, uint32_t taddr,
-//                                                 int row_in_tile, int N);
+//                                                 int row_in_tile, EpiCtx&);
 // taddr addresses this thread's lane (= tile row) at the accumulator's column 0.
 template <int BN, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-               GemmShape shape, typename Epi::Params ep) {
+               const __grid_constant__ CUtensorMap tmap_d, GemmShape shape, typename Epi::Params ep) {
   using S = GemmSmem<BN>;
   constexpr int STAGES = S::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -166,6 +179,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
+    ptx::prefetch_tmap(&tmap_d);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -270,6 +284,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    EpiCtx ctx{&tmap_d, ptx::smem_u32(smem + STAGES * S::kStageBytes + quad * kOutChunkBytes), lane, quad, false};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -281,12 +296,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       }
       ptx::tc_fence_after();
       const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
-      Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile,
-                            shape.N);
+      Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile, ctx);
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[acc]));
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    // bulk stores read shared memory and write global memory asynchronously:
+    // both must be done before the CTA exits
+    if (lane == 0 && ctx.pending) ptx::bulk_wait_all();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
