@@ -301,6 +301,8 @@ def main():
     out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
 
+    y_perm = x_perm   # y_perm reuses x_perm's memory, as in moe_forward
+
     def step(ev=None):
         # exactly moe_forward's sequence, with an event between stages
         moe.moe_clear_device_status(ws)
@@ -311,9 +313,9 @@ def main():
         if ev: ev[2].record(stream)
         moe.moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws)
         if ev: ev[3].record(stream)
-        moe.moe_expert_gemm2(dims, act, offsets, w_down, x_perm, ws)   # y_perm aliases x_perm
+        moe.moe_expert_gemm2(dims, act, offsets, w_down, y_perm, ws)
         if ev: ev[4].record(stream)
-        moe.moe_combine(dims, x_perm, row_of, gate, out)
+        moe.moe_combine(dims, y_perm, row_of, gate, out)
         if ev: ev[5].record(stream)
 
     def barrier():
@@ -411,6 +413,7 @@ def main():
         "gemm1_tflops": g1_tf, "gemm2_tflops": g2_tf,
         "router_tflops": alg["router_flops"] / (stage_ms["route"] * 1e-3) / 1e12,
         "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm"],
+        "permute_note": "dispatch stage (histogram, scan, rank assignment and the row gather)",
         "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm"],
         "roofline": {"kernel": "expert GEMM-1 + SwiGLU (gemm_tc_kernel<256, EpiSwiGLU>)", "bound": "tensor",
                      "achieved": g1_tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": g1_tf / pk["bf16_sus"],

@@ -63,6 +63,8 @@ _SIGS = {
     "moe_prepare_weights": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_dispatch_indices": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_expert_gemm1_gather": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_gemm1": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -190,6 +192,19 @@ def moe_dispatch(dims, x, topk_idx, offsets, row_of, src_token, x_perm, ws, stre
     _dev(topk_idx, offsets, row_of, src_token, dtype=torch.int32)
     _check(lib().moe_dispatch(ctypes.byref(dims), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
                               _ptr(src_token), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_indices(dims, topk_idx, offsets, row_of, src_token, ws, stream=None) -> None:
+    _dev(topk_idx, offsets, row_of, src_token, dtype=torch.int32)
+    _check(lib().moe_dispatch_indices(ctypes.byref(dims), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
+                                      _ptr(src_token), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch_indices")
+
+
+def moe_expert_gemm1_gather(dims, x, src_token, offsets, w13, act, ws, stream=None) -> None:
+    _dev(x, w13, act, dtype=torch.bfloat16)
+    _dev(src_token, offsets, dtype=torch.int32)
+    _check(lib().moe_expert_gemm1_gather(ctypes.byref(dims), _ptr(x), _ptr(src_token), _ptr(offsets), _ptr(w13),
+                                         _ptr(act), _ptr(ws), ws.numel(), _stream(stream)), "moe_expert_gemm1_gather")
 
 
 def moe_dispatch_noalloc(dims, x, topk_idx, offsets, row_of, src_token, x_perm, status=None, stream=None) -> None:

@@ -122,6 +122,23 @@ int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
                      : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream);
 }
 
+// Expert GEMM-1 with the row gather fused into the A loads: A row r is
+// x[src_token[r]], fetched four rows at a time by TMA tile::gather4, so the
+// permuted copy x_perm never exists.
+int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream) {
+  CUtensorMap ta, tb, td;
+  const int rows = static_cast<int>(a.rows);
+  const int n = 2 * a.I;
+  const int bn = (n % 256 == 0) ? 256 : 128;
+  if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, 1)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&td, a.act, a.I, a.rows, kBK, 32)) return MOE_ERR_CUDA;
+  GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status, a.src_token};
+  EpiSwiGLU::Params ep{a.act, a.I};
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream)
+                     : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream);
+}
+
 // Expert GEMM-2 over ragged groups: y_perm = act Wd^T.
 int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb, td;

@@ -45,6 +45,10 @@ struct GemmShape {
   const int* offsets;  // device [groups + 1], or nullptr: one group of rows [0, M)
   int M;            // rows when offsets == nullptr; row capacity of A otherwise
   int* status;      // device status word
+  // Row gather for A: if non-null, logical A row r is row a_gather[r] of the
+  // tensor behind tmap_a (a [*, K] matrix whose map has a 64 x 1 box), loaded
+  // with TMA tile::gather4 by the whole producer warp.
+  const int* a_gather;
 };
 
 template <int BN>
@@ -189,7 +193,60 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   const int total = s_total;
   const int num_kb = shape.K / kBK;
 
-  if (warp == 0) {
+  if (warp == 0 && shape.a_gather != nullptr) {
+    // ------------------------------------------------------ producer (gather)
+    // Lane l owns A rows 4l .. 4l+3 of every tile: it looks up their source
+    // rows once per tile and issues one gather4 per k-block; lane 0 also
+    // waits for free slots, posts the expected bytes and loads B.
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t filled = 0, last_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
+      const int b_row = c.group * shape.N + c.n_blk * BN;
+      int src[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = c.row0 + 4 * lane + j;
+        src[j] = row < c.row_end ? __ldg(shape.a_gather + row) : 0;
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        bool got = true;
+        if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, kWaitLimitNs);
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
+        const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
+        const int k = kb * kBK;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, S::kStageBytes);
+        __syncwarp();
+        ptx::tma_gather4(sa + static_cast<uint32_t>(lane) * 512u, &tmap_a, k, src[0], src[1], src[2], src[3], fb);
+        if (lane == 0) {
+          ptx::tma_load_2d(sa + S::kABytes, &tmap_b, k % shape.K_B, b_row, fb, ptx::policy_evict_last());
+          filled |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {
+        atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        s_abort = 1;
+      }
+      for (int s = 0; s < STAGES; ++s) {
+        if (filled & (1u << s)) {
+          const volatile int never = 0;
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, kWaitLimitNs))
+            atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       const uint64_t pol_a = ptx::policy_evict_normal();

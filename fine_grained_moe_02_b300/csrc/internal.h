@@ -41,6 +41,9 @@ struct RouteArgs {
 };
 
 struct FfnArgs {
+  const uint16_t* x;         // [T, d], gathered GEMM-1 only
+  const int32_t* src_token;  // [rows], gathered GEMM-1 only
+  int64_t T;
   const uint16_t* x_perm;
   const int32_t* offsets;
   const uint16_t* w13;
@@ -68,6 +71,7 @@ size_t dispatch_scratch_bytes(int64_t T, int E);
 int launch_route(const RouteArgs& a, cudaStream_t stream);
 int launch_gemm1(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm2(const FfnArgs& a, cudaStream_t stream);
+int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream);
 int launch_combine(const CombineArgs& a, cudaStream_t stream);
 int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w13, int E, int I, int d,
                        cudaStream_t stream);

@@ -226,6 +226,36 @@ int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_id
   return launch_dispatch(a, static_cast<cudaStream_t>(stream));
 }
 
+int moe_dispatch_indices(const moe_dims* dims, const int32_t* topk_idx, int32_t* offsets, int32_t* row_of,
+                         int32_t* src_token, void* ws, size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (topk_idx == nullptr || offsets == nullptr || row_of == nullptr || src_token == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(topk_idx) || !aligned16(offsets) || !aligned16(row_of) || !aligned16(src_token) || !aligned16(ws))
+    return MOE_ERR_MISALIGNED;
+  const ScratchLayout sl = scratch_layout(dims);
+  if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int64_t nblk_e = static_cast<int64_t>(dispatch_scratch_bytes(dims->T, dims->E) / 8);
+  DispatchArgs a{};
+  a.topk_idx = topk_idx;
+  a.T = dims->T;
+  a.d = dims->d;
+  a.k = dims->top_k;
+  a.E = dims->E;
+  a.offsets = offsets;
+  a.row_of = row_of;
+  a.src_token = src_token;
+  a.x_perm = nullptr;
+  a.block_counts = at<int32_t>(ws, sl.disp);
+  a.block_base = at<int32_t>(ws, sl.disp) + nblk_e;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_dispatch(a, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"
 
 namespace {
@@ -265,6 +295,22 @@ int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t
   a.w13 = w13;
   a.act = act;
   return launch_gemm1(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_gemm1_gather(const moe_dims* dims, const moe_bf16* x, const int32_t* src_token,
+                            const int32_t* offsets, const moe_bf16* w13, moe_bf16* act, void* ws, size_t ws_bytes,
+                            void* stream) {
+  FfnArgs a;
+  int rc = ffn_args(dims, offsets, ws, ws_bytes, a);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || src_token == nullptr || w13 == nullptr || act == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(src_token) || !aligned16(w13) || !aligned16(act)) return MOE_ERR_MISALIGNED;
+  a.x = x;
+  a.T = dims->T;
+  a.src_token = src_token;
+  a.w13 = w13;
+  a.act = act;
+  return launch_gemm1_gather(a, static_cast<cudaStream_t>(stream));
 }
 
 int moe_expert_gemm2(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets, const moe_bf16* w_down,
@@ -340,11 +386,16 @@ int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, 
   int32_t* src = at<int32_t>(ws, f.src);
   moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
   moe_bf16* act = at<moe_bf16>(ws, f.act);
+  // y_perm reuses x_perm's memory: x_perm is dead once expert GEMM-1 has run.
+  // (moe_expert_gemm1_gather would skip x_perm entirely, but on B300 its
+  // four-row TMA gathers are issue-bound and GEMM-1 runs ~3x slower, more
+  // than the ~1.2 ms the separate gather costs on the clip workload.)
+  moe_bf16* yperm = xperm;
   if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
-  if ((rc = moe_expert_ffn(dims, xperm, offsets, w13, w_down, act, xperm, ws, ws_bytes, stream)) != MOE_OK)
-    return rc;
-  return moe_combine(dims, xperm, row_of, gate, out, stream);
+  if ((rc = moe_expert_gemm1(dims, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  return moe_combine(dims, yperm, row_of, gate, out, stream);
 }
 
 int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* w_lat, const moe_bf16* w_head,

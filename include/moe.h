@@ -163,6 +163,11 @@ int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* 
                    const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* The permutation of moe_dispatch without the row gather (offsets, row_of,
+ * src_token only), for use with moe_expert_gemm1_gather. */
+int moe_dispatch_indices(const moe_dims* dims, const int32_t* topk_idx, int32_t* offsets, int32_t* row_of,
+                         int32_t* src_token, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_dispatch for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point.
  *
@@ -195,6 +200,17 @@ int moe_dispatch_noalloc(const moe_dims* dims, const moe_bf16* x, const int32_t*
  * moe_expert_ffn. */
 int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets, const moe_bf16* w13,
                      moe_bf16* act, void* ws, size_t ws_bytes, void* stream);
+/* moe_expert_gemm1 with the sorting gather fused into the operand loads:
+ * row r of the A operand is x[src_token[r]] (x [T, d], src_token from
+ * moe_dispatch / moe_dispatch_indices), fetched by the tensor-memory
+ * accelerator four rows at a time, so x_perm is never materialised (saves
+ * T*top_k*d*2 bytes of memory and the gather's HBM round trip).  The result
+ * equals moe_expert_gemm1 on the gathered x_perm bit for bit.  On B300 the
+ * per-row gathers make this ~3x slower than moe_dispatch + moe_expert_gemm1,
+ * so moe_forward does not use it. */
+int moe_expert_gemm1_gather(const moe_dims* dims, const moe_bf16* x, const int32_t* src_token,
+                            const int32_t* offsets, const moe_bf16* w13, moe_bf16* act, void* ws, size_t ws_bytes,
+                            void* stream);
 int moe_expert_gemm2(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets, const moe_bf16* w_down,
                      moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream);
 

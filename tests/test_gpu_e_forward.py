@@ -76,3 +76,23 @@ def test_forward_host_buffers():
     oh = torch.empty_like(xh).pin_memory()
     moe.moe_forward_host(dev.dims, xh, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, oh, ws)
     assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("kw", [dict(T=3000, d=512, E=32, inter=256), dict(T=77, d=4096, E=8, inter=1024),
+                                dict(T=1, d=512, E=16, inter=128)])
+def test_gathered_gemm1_equals_gemm1_on_x_perm(kw):
+    inp = G.small_inputs(**kw)
+    dev = G.Dev(inp)
+    cfg = inp["cfg"]
+    idx, gate, _ = dev.route(want_logits=False)
+    offsets, row_of, src, x_perm = dev.dispatch(idx)
+    act_ref, _ = dev.ffn(x_perm, offsets)
+    off2 = torch.empty_like(offsets)
+    row2 = torch.empty_like(row_of)
+    src2 = torch.empty_like(src)
+    moe.moe_dispatch_indices(dev.dims, idx, off2, row2, src2, dev.ws)
+    assert torch.equal(off2, offsets) and torch.equal(row2, row_of) and torch.equal(src2, src)
+    act = torch.full_like(act_ref, float("nan"))
+    moe.moe_expert_gemm1_gather(dev.dims, dev.x, src, offsets, dev.w13, act, dev.ws)
+    assert dev.status() == 0
+    assert torch.equal(act.view(torch.int16), act_ref.view(torch.int16))
