@@ -361,6 +361,30 @@ def main():
     barrier()
     fwd_ms = a0.elapsed_time(a1) / n_fwd
 
+    # the folded-router variant of the layer (moe_forward_folded), same workload
+    w_router = torch.empty((E, 2 * d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_prepare_router(dims, w_lat, w_head, w_router)
+    for _ in range(3):
+        moe.moe_forward_folded(dims, x, w_router, bias, w13, w_down, out, ws)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_fold = max(3, args.steps // 2)
+    barrier()
+    f0.record(stream)
+    for _ in range(n_fold):
+        moe.moe_forward_folded(dims, x, w_router, bias, w13, w_down, out, ws)
+    f1.record(stream)
+    barrier()
+    fold_ms = max_over_ranks(f0.elapsed_time(f1) / n_fold, world, "cuda")
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(n_fold):
+        moe.moe_route_folded(dims, x, w_router, bias, idx, gate, None, ws)
+    r1.record(stream)
+    barrier()
+    fold_route_ms = r0.elapsed_time(r1) / n_fold
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status set by the folded-router variant")
+
     # end to end through the public host-buffer entry point
     e2e = None
     if not args.no_e2e:
@@ -420,6 +444,12 @@ def main():
                      "peak_kind": f"bf16 dense sustained ({tag}; kernel timed inside a long step)",
                      "traffic": traffic, "traffic_note": traffic_note,
                      "algorithmic_flops_per_launch": alg["gemm1_flops"]},
+        "variants": {"folded_router": {
+            "value": throughput(T, world, 1, fold_ms / 1e3), "unit": "tokens/s", "ms_per_step": fold_ms,
+            "route_ms": fold_route_ms,
+            "router_tflops": 2 * T * (2 * d) * E / (fold_route_ms * 1e-3) / 1e12,
+            "path": "moe_forward_folded: router folded to s = x (W_head W_lat)^T + b, one bf16 hi/lo GEMM "
+                    "(same outputs and tolerances; h never formed)"}},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
         "e2e": e2e,

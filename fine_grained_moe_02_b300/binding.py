@@ -62,6 +62,9 @@ _SIGS = {
     "moe_get_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_prepare_weights": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_prepare_router": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
+    "moe_route_folded": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_folded": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_dispatch_indices": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_gemm1_gather": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -185,6 +188,29 @@ def moe_route(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, str
     _dev(topk_idx, dtype=torch.int32)
     _check(lib().moe_route(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(topk_idx),
                            _ptr(topk_gate), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def moe_prepare_router(dims, w_lat, w_head, w_router, stream=None) -> None:
+    _dev(w_lat, w_head, w_router, dtype=torch.bfloat16)
+    _check(lib().moe_prepare_router(ctypes.byref(dims), _ptr(w_lat), _ptr(w_head), _ptr(w_router), _stream(stream)),
+           "moe_prepare_router")
+
+
+def moe_route_folded(dims, x, w_router, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _dev(x, w_router, dtype=torch.bfloat16)
+    _dev(bias, topk_gate, logits, dtype=torch.float32)
+    _dev(topk_idx, dtype=torch.int32)
+    _check(lib().moe_route_folded(ctypes.byref(dims), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
+                                  _ptr(topk_gate), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_route_folded")
+
+
+def moe_forward_folded(dims, x, w_router, bias, w13, w_down, out, ws, stream=None) -> None:
+    _dev(x, w_router, w13, w_down, out, dtype=torch.bfloat16)
+    _dev(bias, dtype=torch.float32)
+    _check(lib().moe_forward_folded(ctypes.byref(dims), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w13),
+                                    _ptr(w_down), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_forward_folded")
 
 
 def moe_dispatch(dims, x, topk_idx, offsets, row_of, src_token, x_perm, ws, stream=None) -> None:

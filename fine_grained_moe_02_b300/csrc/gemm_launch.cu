@@ -107,6 +107,20 @@ int launch_route(const RouteArgs& a, cudaStream_t stream) {
   }
 }
 
+// Folded router: s = [x | x] w_router^T + bias (K = 2d; w_router = [W_eff hi | lo])
+// with the top-k epilogue.
+int launch_route_folded(const RouteArgs& a, const uint16_t* w_router, cudaStream_t stream) {
+  const int64_t m_tiles = (a.T + kBM - 1) / kBM;
+  const int bn = a.E <= 16 ? 16 : a.E <= 32 ? 32 : a.E <= 64 ? 64 : a.E <= 128 ? 128 : 256;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, w_router, 2ULL * a.d, a.E, kBK, bn)) return MOE_ERR_CUDA;
+  GemmShape sh{2 * a.d, 2 * a.d, bn, 1, nullptr, static_cast<int>(a.T), a.status, nullptr, a.d};
+  EpiTopK::Params ep{a.bias, a.logits, a.topk_idx, a.topk_gate, a.E, a.k};
+  const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
+  return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream);
+}
+
 // Expert GEMM-1 over ragged groups (device offsets), SwiGLU fused: act = silu(x Wg^T) * (x Wu^T).
 int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb, td;

@@ -49,6 +49,9 @@ struct GemmShape {
   // tensor behind tmap_a (a [*, K] matrix whose map has a 64 x 1 box), loaded
   // with TMA tile::gather4 by the whole producer warp.
   const int* a_gather;
+  // A's k coordinate is k % K_A (0 means K): one A tile serves a K = c*K_A
+  // sweep (the folded router reads x twice, against W_eff's hi and lo halves).
+  int K_A;
 };
 
 template <int BN>
@@ -269,7 +272,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
           const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
           const uint32_t sb = sa + S::kABytes;
           const int k = kb * kBK;
-          ptx::tma_load_2d(sa, &tmap_a, k, c.row0, fb, pol_a);
+          ptx::tma_load_2d(sa, &tmap_a, shape.K_A > 0 ? k % shape.K_A : k, c.row0, fb, pol_a);
           ptx::tma_load_2d(sb, &tmap_b, k % shape.K_B, b_row, fb, pol_b);
           filled |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);

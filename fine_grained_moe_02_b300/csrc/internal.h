@@ -69,6 +69,9 @@ struct CombineArgs {
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 size_t dispatch_scratch_bytes(int64_t T, int E);
 int launch_route(const RouteArgs& a, cudaStream_t stream);
+int launch_route_folded(const RouteArgs& a, const uint16_t* w_router, cudaStream_t stream);
+int launch_fold_router(const uint16_t* w_head, const uint16_t* w_lat, int E, int L, int d, uint16_t* w_router,
+                       cudaStream_t stream);
 int launch_gemm1(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm2(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream);

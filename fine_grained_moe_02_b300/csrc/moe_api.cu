@@ -193,6 +193,44 @@ int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, co
   return launch_route(a, static_cast<cudaStream_t>(stream));
 }
 
+int moe_prepare_router(const moe_dims* dims, const moe_bf16* w_lat, const moe_bf16* w_head, moe_bf16* w_router,
+                       void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (w_lat == nullptr || w_head == nullptr || w_router == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_lat) || !aligned16(w_head) || !aligned16(w_router)) return MOE_ERR_MISALIGNED;
+  return launch_fold_router(w_head, w_lat, dims->E, dims->n_heads * dims->head_dim, dims->d, w_router,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int moe_route_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                     int32_t* topk_idx, float* topk_gate, float* logits, void* ws, size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_router == nullptr || topk_idx == nullptr || topk_gate == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) || !aligned16(ws) ||
+      (bias != nullptr && !aligned16(bias)) || (logits != nullptr && !aligned16(logits)))
+    return MOE_ERR_MISALIGNED;
+  if (ws_bytes < scratch_layout(dims).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  RouteArgs a{};
+  a.x = x;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_gate = topk_gate;
+  a.logits = logits;
+  a.T = dims->T;
+  a.d = dims->d;
+  a.L = dims->n_heads * dims->head_dim;
+  a.E = dims->E;
+  a.k = dims->top_k;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_route_folded(a, w_router, static_cast<cudaStream_t>(stream));
+}
+
 int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_idx, int32_t* offsets,
                  int32_t* row_of, int32_t* src_token, moe_bf16* x_perm, void* ws, size_t ws_bytes, void* stream) {
   int rc = moe_check_dims(dims);
@@ -396,6 +434,34 @@ int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, 
   if ((rc = moe_expert_gemm1(dims, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
   return moe_combine(dims, yperm, row_of, gate, out, stream);
+}
+
+int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                       const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws, size_t ws_bytes,
+                       void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_router == nullptr || w13 == nullptr || w_down == nullptr || out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w13) || !aligned16(w_down) || !aligned16(out) ||
+      !aligned16(ws) || (bias != nullptr && !aligned16(bias)))
+    return MOE_ERR_MISALIGNED;
+  const ForwardLayout f = forward_layout(dims);
+  if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
+  int32_t* idx = at<int32_t>(ws, f.idx);
+  float* gate = at<float>(ws, f.gate);
+  int32_t* offsets = at<int32_t>(ws, f.offsets);
+  int32_t* row_of = at<int32_t>(ws, f.row_of);
+  int32_t* src = at<int32_t>(ws, f.src);
+  moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
+  moe_bf16* act = at<moe_bf16>(ws, f.act);
+  if ((rc = moe_route_folded(dims, x, w_router, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK)
+    return rc;
+  if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm1(dims, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  return moe_combine(dims, xperm, row_of, gate, out, stream);
 }
 
 int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* w_lat, const moe_bf16* w_head,

@@ -136,6 +136,20 @@ int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, co
               const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
               void* ws, size_t ws_bytes, void* stream);
 
+/* Folded router (optional fast path).  The summed head scores are linear in
+ * x: s = x (W_head W_lat)^T + b.  moe_prepare_router computes
+ * W_eff = W_head W_lat [E, d] once per weight load (fp32 accumulation) and
+ * stores it as a bf16 pair: w_router [E, 2d], row e = [bf16(W_eff[e]) |
+ * bf16(W_eff[e] - hi)].  moe_route_folded then evaluates s with one bf16
+ * tensor-core GEMM of K = 2d against [x | x] and applies the same bias,
+ * softmax, top-k and gates as moe_route (same outputs, same tolerances);
+ * the latent vector h is never formed.  Router work on the clip workload
+ * drops from 2.88 to 0.23 TFLOP.  Arguments as in moe_route. */
+int moe_prepare_router(const moe_dims* dims, const moe_bf16* w_lat, const moe_bf16* w_head, moe_bf16* w_router,
+                       void* stream);
+int moe_route_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                     int32_t* topk_idx, float* topk_gate, float* logits, void* ws, size_t ws_bytes, void* stream);
+
 /* Sorting: counting-sort permutation of the T*top_k (token, slot) pairs into
  * expert-contiguous order, then the row gather.
  *   topk_idx  [T, top_k] int32 (read)
@@ -230,6 +244,11 @@ int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row
 int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out,
                 void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward with the folded router (w_router from moe_prepare_router). */
+int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                       const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws, size_t ws_bytes,
+                       void* stream);
 
 /* moe_forward for a caller whose activations live in host memory: copies
  * x_host [T, d] to the device, runs the layer, copies out to out_host [T, d]

@@ -3,9 +3,12 @@ stages, and compare against the fp64 oracle with the layer's parity bars.
 
 Parity bars (fixed by the layer's specification):
   * router logits: max-abs error <= 1e-3
-  * expert indices and the permutation: bit-exact wherever the oracle's
-    k-th to (k+1)-th logit margin exceeds 1e-3; on near-tie tokens the GPU's
-    set must be a valid top-k (each chosen logit >= oracle k-th logit - 2e-3)
+  * expert indices and the permutation: the chosen set bit-exact wherever the
+    oracle's k-th to (k+1)-th logit margin exceeds 1e-3, the slot order
+    bit-exact where adjacent in-set gaps also exceed 2e-3 (otherwise a valid
+    descending order); on near-tie tokens the GPU's set must be a valid top-k
+    (each chosen logit >= oracle k-th logit - 2e-3); the permutation
+    bit-exact against the oracle's counting sort of the GPU's ids
   * layer output: relative Frobenius error <= 1e-2 and max-abs <= 5e-2
   * gates: max-abs <= 1e-3 (diagnostic), sum to 1 within 1e-6
 """
@@ -118,7 +121,15 @@ def check_routing(s_ref: np.ndarray, idx_gpu: np.ndarray, gate_gpu: np.ndarray, 
     srt = np.sort(s_ref, axis=1)[:, ::-1]
     margin = srt[:, k - 1] - srt[:, k] if k < E else np.full(T, np.inf)
     clear = margin > MARGIN
-    np.testing.assert_array_equal(idx_gpu[clear], idx_ref[clear])
+    # the chosen set is unique where the k-th/(k+1)-th margin exceeds the bar
+    np.testing.assert_array_equal(np.sort(idx_gpu[clear], 1), np.sort(idx_ref[clear], 1))
+    # slot order: unique where every adjacent gap inside the top-k exceeds two
+    # logit tolerances; elsewhere it must be a valid descending order
+    gaps = -np.diff(srt[:, :k], axis=1) if k > 1 else np.full((T, 1), np.inf)
+    ordered = clear & np.all(gaps > 2 * LOGIT_TOL, axis=1)
+    np.testing.assert_array_equal(idx_gpu[ordered], idx_ref[ordered])
+    along = np.take_along_axis(s_ref, np.clip(idx_gpu, 0, E - 1).astype(np.int64), 1)
+    assert np.all(np.diff(along, axis=1) <= 2 * LOGIT_TOL)
     # near ties: a valid top-k with distinct in-range ids
     assert np.all((idx_gpu >= 0) & (idx_gpu < E))
     for t in np.nonzero(~clear)[0]:
