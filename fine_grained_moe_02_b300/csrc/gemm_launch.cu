@@ -166,6 +166,22 @@ int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
   return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream);
 }
 
+// Self-test of the bounded waits: one 128 x 256 x 64 tile whose producer
+// issues nothing, so the MMA and epilogue waits run out after `limit_ns`.
+// Operands and output live in `scratch` (>= 112 KB); nothing is loaded or stored.
+int launch_selftest_timeout(uint16_t* scratch, int* status, uint64_t limit_ns, cudaStream_t stream) {
+  CUtensorMap ta, tb, td;
+  uint16_t* a = scratch;                 // [128, 64]
+  uint16_t* b = scratch + 128 * 64;      // [256, 64]
+  uint16_t* d = scratch + 384 * 64;      // [128, 256]
+  if (!make_tmap_bf16_2d(&ta, a, 64, 128, kBK, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, b, 64, 256, kBK, 256)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&td, d, 256, 128, kBK, 32)) return MOE_ERR_CUDA;
+  GemmShape sh{64, 64, 256, 1, nullptr, 128, status, nullptr, 0, limit_ns, 1};
+  EpiStoreBf16::Params ep{d, 256};
+  return run_gemm<256, EpiStoreBf16>(ta, tb, td, sh, ep, 1, stream);
+}
+
 // w13[e, 128b + j] = j < 64 ? w_gate[e, 64b + j] : w_up[e, 64b + j - 64]   (rows of d)
 __global__ void __launch_bounds__(256) prepare_w13_kernel(const uint4* __restrict__ wg, const uint4* __restrict__ wu,
                                                           uint4* __restrict__ w13, int64_t n_rows, int I,

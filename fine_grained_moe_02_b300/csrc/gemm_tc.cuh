@@ -52,6 +52,11 @@ struct GemmShape {
   // A's k coordinate is k % K_A (0 means K): one A tile serves a K = c*K_A
   // sweep (the folded router reads x twice, against W_eff's hi and lo halves).
   int K_A;
+  // Limit of every pipeline wait (0: kWaitLimitNs).
+  uint64_t wait_limit_ns;
+  // Self-test only: the producer issues no loads, so the other roles' waits
+  // run out and the timeout path (status bit, drain, TMEM release) executes.
+  int selftest_stall;
 };
 
 template <int BN>
@@ -195,6 +200,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   const uint32_t tmem_base = s_tmem;
   const int total = s_total;
   const int num_kb = shape.K / kBK;
+  const uint64_t wait_ns = shape.wait_limit_ns ? shape.wait_limit_ns : kWaitLimitNs;
 
   if (warp == 0 && shape.a_gather != nullptr) {
     // ------------------------------------------------------ producer (gather)
@@ -216,7 +222,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       }
       for (int kb = 0; kb < num_kb; ++kb) {
         bool got = true;
-        if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, kWaitLimitNs);
+        if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, wait_ns);
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
           ok = false;
           break;
@@ -243,7 +249,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       for (int s = 0; s < STAGES; ++s) {
         if (filled & (1u << s)) {
           const volatile int never = 0;
-          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, kWaitLimitNs))
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, wait_ns))
             atomicOr(shape.status, MOE_DEV_TIMEOUT);
         }
       }
@@ -259,11 +265,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       uint32_t filled = 0;       // bit s: stage s was filled at least once
       uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < total && ok && !shape.selftest_stall; tile += gridDim.x) {
         const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
         const int b_row = c.group * shape.N + c.n_blk * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, kWaitLimitNs)) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, wait_ns)) {
             ok = false;
             break;
           }
@@ -287,7 +293,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       for (int s = 0; s < STAGES; ++s) {
         if (filled & (1u << s)) {
           const volatile int never = 0;
-          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, kWaitLimitNs))
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, wait_ns))
             atomicOr(shape.status, MOE_DEV_TIMEOUT);
         }
       }
@@ -302,14 +308,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), acc_phase ^ 1, &s_abort, kWaitLimitNs)) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), acc_phase ^ 1, &s_abort, wait_ns)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::kAccStride);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, &s_abort, kWaitLimitNs)) {
+          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[stage]), phase, &s_abort, wait_ns)) {
             ok = false;
             break;
           }
@@ -336,7 +342,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       // drain: all MMAs issued by this thread complete before TMEM is freed
       ptx::mma_commit(ptx::smem_u32(&drain_bar));
       const volatile int never = 0;
-      if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, &never, kWaitLimitNs))
+      if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, &never, wait_ns))
         atomicOr(shape.status, MOE_DEV_TIMEOUT);
     }
   } else {
@@ -348,7 +354,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const bool ok = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, kWaitLimitNs);
+      const bool ok = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) atomicOr(shape.status, MOE_DEV_TIMEOUT);
         s_abort = 1;

@@ -112,6 +112,15 @@ int moe_clear_device_status(void* ws, void* stream);
  * not (the word is left as is), MOE_ERR_CUDA if the sync failed. */
 int moe_get_device_status(void* ws, int32_t* status, void* stream);
 
+/* Self-test of device-side failure detection: runs the tensor-core GEMM
+ * kernel on one tile with its loader told to issue nothing, so the kernel's
+ * pipeline waits run out after limit_us microseconds (1 .. 10^7).  The
+ * kernel then sets MOE_DEV_TIMEOUT in the status word of `ws`, releases its
+ * tensor memory and returns; nothing faults and the context stays usable.
+ * Uses the first 1 KB + 112 KB of `ws` (ws_bytes >= 129 KB).  Read the
+ * result with moe_get_device_status. */
+int moe_selftest_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
+
 /* Builds the interleaved gate/up weight used by moe_expert_ffn:
  *   w13[e] is [2*inter, d]; for block b = 0 .. inter/64 - 1 its rows
  *   [128b, 128b+64) are w_gate[e][64b, 64b+64) and rows [128b+64, 128b+128)

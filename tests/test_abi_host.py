@@ -83,3 +83,11 @@ def test_null_and_misaligned_pointers_are_rejected_on_the_host(L):
     d0 = moe.moe_dims.make(256, 500, 16, 128)
     assert L.moe_route(ctypes.byref(d0), ok, ok, ok, nul, ok, ok, nul, ok, 1 << 30, nul) == B.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_check_dims(None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_selftest_argument_checks(L):
+    P = ctypes.c_void_p(0x10000)
+    assert L.moe_selftest_timeout(None, 1 << 20, 1000, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_timeout(P, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_timeout(ctypes.c_void_p(0x10008), 1 << 20, 1000, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_selftest_timeout(P, 4096, 1000, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL

@@ -96,3 +96,19 @@ def test_gathered_gemm1_equals_gemm1_on_x_perm(kw):
     moe.moe_expert_gemm1_gather(dev.dims, dev.x, src, offsets, dev.w13, act, dev.ws)
     assert dev.status() == 0
     assert torch.equal(act.view(torch.int16), act_ref.view(torch.int16))
+
+
+def test_pipeline_wait_timeout_is_reported_and_the_context_survives():
+    # the loader issues nothing: the kernel's waits run out after 20 ms
+    ws = moe.alloc_workspace(1 << 20)
+    moe.moe_clear_device_status(ws)
+    moe.moe_selftest_timeout(ws, 20_000)
+    assert moe.moe_get_device_status(ws) & moe.binding.MOE_DEV_TIMEOUT
+    # the GPU still computes correctly afterwards (tensor memory was released)
+    inp = mi.make_inputs("tiny")
+    dev = G.Dev(inp)
+    idx, gate, _ = dev.route(want_logits=False)
+    out = dev.forward()
+    assert dev.status() == 0
+    ref = O.forward_bits(inp, topk_idx=idx.cpu().numpy())
+    G.check_out(G.host_f64(out), ref["out"])
