@@ -258,7 +258,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      const uint64_t pol_a = ptx::policy_evict_normal();
+      // Both operands evict_last: an A tile is read by the n_tiles CTAs that
+      // share its rows at slightly different times and must survive until the
+      // last one (with evict_normal on A, expert GEMM-1 on the clip workload
+      // re-read 22% of x_perm from DRAM); B is reused by every m-block of the group.
+      const uint64_t pol_a = ptx::policy_evict_last();
       const uint64_t pol_b = ptx::policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
