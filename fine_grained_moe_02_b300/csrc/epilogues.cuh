@@ -176,77 +176,86 @@ struct EpiHiLo {
   }
 };
 
-// Router stage 2: summed head scores (fp32 accumulator, all E experts in one
-// tile) -> + bias -> optional logits store -> top-k (value descending, ties
-// to the lower expert index) -> softmax over the chosen k.
-struct EpiTopK {
-  struct Params {
-    const float* bias;  // [E] or nullptr
-    float* logits;      // [T, E] or nullptr
-    int32_t* idx;       // [T, k]
-    float* gate;        // [T, k]
-    int E;
-    int k;
-  };
-  template <int BN>
-  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
-                                             EpiCtx&) {
-    const int row = c.row0 + r;
-    const bool valid = row < c.row_end;
-    float bv[kMaxTopK];
-    int bi[kMaxTopK];
+// Summed head scores of one token (its TMEM lane, columns 0 .. E-1 from taddr)
+// -> + bias -> optional logits row -> top-k (value descending, ties to the
+// lower expert index) -> softmax over the chosen k -> idx/gate rows.  All 32
+// lanes of the warp must call it (the TMEM loads are warp-collective).
+struct TopKParams {
+  const float* bias;  // [E] or nullptr
+  float* logits;      // [T, E] or nullptr
+  int32_t* idx;       // [T, k]
+  float* gate;        // [T, k]
+  int E;
+  int k;
+};
+
+template <int BN>
+__device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, int row, bool valid) {
+  float bv[kMaxTopK];
+  int bi[kMaxTopK];
 #pragma unroll
-    for (int i = 0; i < kMaxTopK; ++i) { bv[i] = -INFINITY; bi[i] = -1; }
-    float* lrow = (p.logits != nullptr && valid) ? p.logits + static_cast<int64_t>(row) * p.E : nullptr;
+  for (int i = 0; i < kMaxTopK; ++i) { bv[i] = -INFINITY; bi[i] = -1; }
+  float* lrow = (p.logits != nullptr && valid) ? p.logits + static_cast<int64_t>(row) * p.E : nullptr;
 #pragma unroll 1
-    for (int col = 0; col < BN; col += 16) {
-      uint32_t u[16];
-      __syncwarp();
-      ptx::tmem_ld16(taddr + col, u);
-      ptx::tmem_ld_wait();
+  for (int col = 0; col < BN; col += 16) {
+    uint32_t u[16];
+    __syncwarp();
+    ptx::tmem_ld16(taddr + col, u);
+    ptx::tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = col + j;
-        if (e < p.E) {
-          float s = __uint_as_float(u[j]);
-          if (p.bias != nullptr) s += __ldg(p.bias + e);
-          if (lrow != nullptr) lrow[e] = s;
-          if (s > bv[kMaxTopK - 1]) {
-            float cv = s;
-            int ci = e;
+    for (int j = 0; j < 16; ++j) {
+      const int e = col + j;
+      if (e < p.E) {
+        float s = __uint_as_float(u[j]);
+        if (p.bias != nullptr) s += __ldg(p.bias + e);
+        if (lrow != nullptr) lrow[e] = s;
+        if (s > bv[kMaxTopK - 1]) {
+          float cv = s;
+          int ci = e;
 #pragma unroll
-            for (int q = 0; q < kMaxTopK; ++q) {
-              const bool gt = cv > bv[q];
-              const float tv = gt ? bv[q] : cv;
-              const int ti = gt ? bi[q] : ci;
-              bv[q] = gt ? cv : bv[q];
-              bi[q] = gt ? ci : bi[q];
-              cv = tv;
-              ci = ti;
-            }
+          for (int q = 0; q < kMaxTopK; ++q) {
+            const bool gt = cv > bv[q];
+            const float tv = gt ? bv[q] : cv;
+            const int ti = gt ? bi[q] : ci;
+            bv[q] = gt ? cv : bv[q];
+            bi[q] = gt ? ci : bi[q];
+            cv = tv;
+            ci = ti;
           }
         }
       }
     }
-    if (!valid) return;
-    const float m = bv[0];
-    float w[kMaxTopK];
-    float sum = 0.f;
+  }
+  if (!valid) return;
+  const float m = bv[0];
+  float w[kMaxTopK];
+  float sum = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxTopK; ++i) {
-      w[i] = (i < p.k) ? expf(bv[i] - m) : 0.f;
-      sum += w[i];
-    }
-    const float inv = 1.0f / sum;
-    int32_t* io = p.idx + static_cast<int64_t>(row) * p.k;
-    float* go = p.gate + static_cast<int64_t>(row) * p.k;
+  for (int i = 0; i < kMaxTopK; ++i) {
+    w[i] = (i < p.k) ? expf(bv[i] - m) : 0.f;
+    sum += w[i];
+  }
+  const float inv = 1.0f / sum;
+  int32_t* io = p.idx + static_cast<int64_t>(row) * p.k;
+  float* go = p.gate + static_cast<int64_t>(row) * p.k;
 #pragma unroll
-    for (int i = 0; i < kMaxTopK; ++i) {
-      if (i < p.k) {
-        io[i] = bi[i];
-        go[i] = w[i] * inv;
-      }
+  for (int i = 0; i < kMaxTopK; ++i) {
+    if (i < p.k) {
+      io[i] = bi[i];
+      go[i] = w[i] * inv;
     }
+  }
+}
+
+// Router stage 2: summed head scores (fp32 accumulator, all E experts in one
+// tile) -> top-k epilogue.
+struct EpiTopK {
+  using Params = TopKParams;
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx&) {
+    const int row = c.row0 + r;
+    topk_row<BN>(p, taddr, row, row < c.row_end);
   }
 };
 

@@ -79,9 +79,15 @@ bool make_tmap_bf16_2d(void* tmap, const void* base, uint64_t cols, uint64_t row
   return r == CUDA_SUCCESS;
 }
 
-// Router: stage 1  hl = [hi | lo](x W_lat^T)            dense GEMM, N = L, fused hi/lo split
+// Router, default path: two tensor-core GEMMs with h in HBM as a bf16 hi/lo
+// pair.  On B300 it beats the on-chip kernel (router_fused.cu, moe_route_fused)
+// because that kernel's per-head conversion of h serialises with its MMAs.
+int launch_route(const RouteArgs& a, cudaStream_t stream) { return launch_route_two_stage(a, stream); }
+
+// Two-stage router (h through HBM as a bf16 hi/lo pair):
+//         stage 1  hl = [hi | lo](x W_lat^T)            dense GEMM, N = L, fused hi/lo split
 //         stage 2  s  = hl [W_head | W_head]^T + bias   dense GEMM, K = 2L, N = E, fused top-k
-int launch_route(const RouteArgs& a, cudaStream_t stream) {
+int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream) {
   const int64_t m_tiles = (a.T + kBM - 1) / kBM;
   CUtensorMap ta, tb, td;
   {

@@ -33,9 +33,11 @@ struct RouteArgs {
   int32_t* topk_idx;
   float* topk_gate;
   float* logits;
-  uint16_t* hl;            // scratch [T, 2L] bf16: latent hi | lo
+  uint16_t* hl;            // scratch [T, 2L] bf16: latent hi | lo (two-stage router)
+  float* partial;          // scratch for the fused router's head-group partial scores (aliases hl)
   int64_t T;
   int d, L, E, k;
+  int head_dim;
   int* status;
   int sm_count;
 };
@@ -69,6 +71,9 @@ struct CombineArgs {
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 size_t dispatch_scratch_bytes(int64_t T, int E);
 int launch_route(const RouteArgs& a, cudaStream_t stream);
+int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream);
+bool route_fused_supported(int head_dim);
+int launch_route_fused(const RouteArgs& a, int head_dim, cudaStream_t stream);
 int launch_route_folded(const RouteArgs& a, const uint16_t* w_router, cudaStream_t stream);
 int launch_fold_router(const uint16_t* w_head, const uint16_t* w_lat, int E, int L, int d, uint16_t* w_router,
                        cudaStream_t stream);

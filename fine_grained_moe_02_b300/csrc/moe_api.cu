@@ -196,9 +196,46 @@ int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, co
   a.L = dims->n_heads * dims->head_dim;
   a.E = dims->E;
   a.k = dims->top_k;
+  a.head_dim = dims->head_dim;
   a.status = status_ptr(ws);
   a.sm_count = sms;
   return launch_route(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_route_fused(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                    const float* bias, int32_t* topk_idx, float* topk_gate, float* logits, void* ws, size_t ws_bytes,
+                    void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (!route_fused_supported(dims->head_dim)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || topk_idx == nullptr || topk_gate == nullptr ||
+      ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(topk_idx) || !aligned16(topk_gate) ||
+      !aligned16(ws) || (bias != nullptr && !aligned16(bias)) || (logits != nullptr && !aligned16(logits)))
+    return MOE_ERR_MISALIGNED;
+  const ScratchLayout sl = scratch_layout(dims);
+  if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  RouteArgs a{};
+  a.x = x;
+  a.w_lat = w_lat;
+  a.w_head = w_head;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_gate = topk_gate;
+  a.logits = logits;
+  a.partial = at<float>(ws, sl.hl);  // [G, T, E] fp32 head-group partial scores, G * E <= L
+  a.T = dims->T;
+  a.d = dims->d;
+  a.L = dims->n_heads * dims->head_dim;
+  a.E = dims->E;
+  a.k = dims->top_k;
+  a.head_dim = dims->head_dim;
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_route_fused(a, dims->head_dim, static_cast<cudaStream_t>(stream));
 }
 
 int moe_prepare_router(const moe_dims* dims, const moe_bf16* w_lat, const moe_bf16* w_head, moe_bf16* w_router,

@@ -145,6 +145,20 @@ int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, co
               const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
               void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route with the latent vector kept on chip: one persistent tensor-core
+ * kernel accumulates each head's 128-token x head_dim block of h in tensor
+ * memory (fp32), converts it to the bf16 hi/lo operand in shared memory and
+ * accumulates the head scores into a second tensor-memory block; only
+ * per-head-group partial scores (G x T x E fp32, G | n_heads) leave the SM,
+ * summed in fixed order by a small selection kernel.  Same outputs and
+ * tolerances as moe_route.  Requires head_dim % 64 == 0 and head_dim <= 256
+ * (else MOE_ERR_UNSUPPORTED_SHAPE).  On B300 it is slower than moe_route
+ * (2.9 vs 2.4 ms on the clip workload): the conversion of h between a head's
+ * latent and score products leaves the tensor cores idle. */
+int moe_route_fused(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                    const float* bias, int32_t* topk_idx, float* topk_gate, float* logits, void* ws, size_t ws_bytes,
+                    void* stream);
+
 /* Folded router (optional fast path).  The summed head scores are linear in
  * x: s = x (W_head W_lat)^T + b.  moe_prepare_router computes
  * W_eff = W_head W_lat [E, d] once per weight load (fp32 accumulation) and

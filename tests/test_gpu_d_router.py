@@ -17,16 +17,26 @@ pytestmark = pytest.mark.gpu
     dict(T=200, d=512, E=6, inter=64, top_k=6),                         # k == E: gates = full softmax
     dict(T=333, d=768, E=40, inter=64, top_k=1),                        # E not a power of two
     dict(T=130, d=128, E=128, inter=64, n_heads=2, head_dim=128),      # other head geometry
+    dict(T=200, d=256, E=32, inter=64, n_heads=4, head_dim=64),        # fused router, small heads
+    dict(T=150, d=512, E=48, inter=64, n_heads=4, head_dim=192),       # fused router, 3 chunks per head
+    dict(T=140, d=256, E=24, inter=64, n_heads=1, head_dim=512),       # two-stage only
+    dict(T=1000, d=1024, E=128, inter=64),                              # on-chip: several head groups
 ])
-def test_router_matches_oracle(kw):
+@pytest.mark.parametrize("path", ["two_stage", "fused"])
+def test_router_matches_oracle(kw, path):
     inp = G.small_inputs(**kw)
+    cfg = inp["cfg"]
     dev = G.Dev(inp)
-    idx, gate, logits = dev.route()
+    if path == "two_stage":
+        idx, gate, logits = dev.route()
+    else:
+        if cfg.head_dim % 64 or cfg.head_dim > 256:
+            pytest.skip("the on-chip router covers head_dim % 64 == 0, <= 256")
+        idx, gate, logits = dev.route_fused()
     assert dev.status() == 0
     s_ref = G.oracle_logits(inp)
-    stats = G.check_routing(s_ref, idx.cpu().numpy(), gate.cpu().numpy(), inp["cfg"].top_k,
-                            logits.cpu().numpy())
-    assert stats["near_ties"] <= max(3, inp["cfg"].T // 50)
+    stats = G.check_routing(s_ref, idx.cpu().numpy(), gate.cpu().numpy(), cfg.top_k, logits.cpu().numpy())
+    assert stats["near_ties"] <= max(3, cfg.T // 50)
 
 
 def test_router_bias_forces_experts():
@@ -47,3 +57,14 @@ def test_router_without_logits_output_gives_same_routing():
     i1, g1, _ = dev.route(want_logits=True)
     i2, g2, _ = dev.route(want_logits=False)
     assert torch.equal(i1, i2) and torch.equal(g1, g2)
+
+
+def test_fused_router_full_clip_sampled():
+    inp = mi.make_inputs("clip")
+    dev = G.Dev(inp)
+    cfg = inp["cfg"]
+    idx, gate, logits = dev.route_fused()
+    assert dev.status() == 0
+    tok = mi.sample_tokens(cfg.T, 512, seed=13)
+    G.check_routing(G.oracle_logits(inp, tok), idx.cpu().numpy()[tok], gate.cpu().numpy()[tok], cfg.top_k,
+                    logits[torch.from_numpy(tok).cuda()].cpu().numpy())
