@@ -46,6 +46,8 @@ class MoeConfig:
     bias: str = "none"               # "none" | "zipf"
     zipf_s: float = 1.2
     modality_split: tuple = ()       # ((n_tokens, x_scale), ...) in sequence order
+    modality_experts: tuple = ()     # ((begin, end), ...) routed experts of each modality; () = no masking
+    n_shared: int = 0                # shared experts, stored after the E routed experts
     seed: int = 0
     note: str = ""
 
@@ -74,12 +76,19 @@ CONFIGS = {
                       note="full 10 s preview clip: 60 latent frames x 1792 tokens, Zipf(1.2) router bias"),
     "refiner": MoeConfig("refiner", T=48960, d=4096, E=256, inter=512, router_init="uniform",
                          note="refiner chunk: 6 latent frames x 68x120 tokens, E=256, inter=512, uniform routing"),
+    # the chunk's video|text|audio stream with modality-specific routed experts
+    # (video 0-95, text 96-111, audio 112-127) and one shared expert
+    "chunk_mm": MoeConfig("chunk_mm", T=10752 + 256 + 384, d=4096, E=128, inter=1024,
+                          modality_split=((10752, 1.0), (256, 0.5), (384, 0.8)),
+                          modality_experts=((0, 96), (96, 112), (112, 128)), n_shared=1,
+                          note="24-frame chunk with modality-specific experts (video 96, text 16, audio 16) "
+                               "and one shared expert"),
     # not one of the pages' workloads: a 4096-token slice at clip width with 32
     # experts, small enough (~1.5 GB on the device) for full profiler captures
     "slice": MoeConfig("slice", T=4096, d=4096, E=32, inter=1024,
                        note="profiling size: 4096 tokens, d=4096, E=32, inter=1024"),
 }
-CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "slice"]
+CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "slice"]
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -235,14 +244,22 @@ def make_weights(cfg: MoeConfig) -> dict:
     w_lat [L, d], w_head [E, L], w_gate/w_up [E, inter, d], w_down [E, d, inter],
     bias [E] float32 or None.
     """
+    n_exp = cfg.E + cfg.n_shared   # shared experts follow the routed ones
     return dict(
         w_lat=_w(cfg, "w_lat", (cfg.L, cfg.d), cfg.d, True),
         w_head=_w(cfg, "w_head", (cfg.E, cfg.L), cfg.head_dim, True),
-        w_gate=_w(cfg, "w_gate", (cfg.E, cfg.inter, cfg.d), cfg.d, False),
-        w_up=_w(cfg, "w_up", (cfg.E, cfg.inter, cfg.d), cfg.d, False),
-        w_down=_w(cfg, "w_down", (cfg.E, cfg.d, cfg.inter), cfg.inter, False),
+        w_gate=_w(cfg, "w_gate", (n_exp, cfg.inter, cfg.d), cfg.d, False),
+        w_up=_w(cfg, "w_up", (n_exp, cfg.inter, cfg.d), cfg.d, False),
+        w_down=_w(cfg, "w_down", (n_exp, cfg.d, cfg.inter), cfg.inter, False),
         bias=router_bias(cfg),
     )
+
+
+def make_modality(cfg: MoeConfig) -> np.ndarray:
+    """Modality id of each token (int32 [T]): its index in modality_split."""
+    if not cfg.modality_split:
+        return np.zeros(cfg.T, dtype=np.int32)
+    return np.concatenate([np.full(n, m, dtype=np.int32) for m, (n, _) in enumerate(cfg.modality_split)])
 
 
 def make_inputs(cfg: MoeConfig | str) -> dict:
@@ -250,6 +267,7 @@ def make_inputs(cfg: MoeConfig | str) -> dict:
         cfg = CONFIGS[cfg]
     out = make_weights(cfg)
     out["x"] = make_x(cfg)
+    out["modality"] = make_modality(cfg)
     out["cfg"] = cfg
     return out
 

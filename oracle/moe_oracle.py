@@ -90,6 +90,8 @@ def topk_select(p: np.ndarray, k: int) -> np.ndarray:
 
     Slot order: value descending, then expert index ascending.  A stable sort
     on -p keeps equal values in index order, so the lowest index wins a tie.
+    Applied to the scores s (or to softmax(s): the same indices, as exp is
+    monotone; s keeps values distinct where exp would underflow to 0).
     """
     order = np.argsort(-p, axis=1, kind="stable")
     return order[:, :k].astype(np.int32)
@@ -106,7 +108,7 @@ def route(x, w_lat, w_head, bias, n_heads: int, head_dim: int, k: int):
     h = latent_projection(x, w_lat)
     s = head_scores(h, w_head, bias, n_heads, head_dim)
     p = softmax(s)
-    idx = topk_select(p, k)
+    idx = topk_select(s, k)   # the k largest p are the k largest s (exp is monotone)
     return s, idx, renormalised_gates(p, idx)
 
 
@@ -216,7 +218,9 @@ def forward(x, w_lat, w_head, bias, w_gate, w_up, w_down, n_heads, head_dim, k,
     """
     s = head_scores(latent_projection(x, w_lat), w_head, bias, n_heads, head_dim)
     p = softmax(s)
-    idx = topk_select(p, k) if topk_idx is None else np.asarray(topk_idx, dtype=np.int32)
+    # select on s: same set as on p, and exp underflow cannot turn distinct
+    # scores into ties
+    idx = topk_select(s, k) if topk_idx is None else np.asarray(topk_idx, dtype=np.int32)
     gates = renormalised_gates(p, idx)
     counts, offsets, row_of, src_token = dispatch(idx, w_head.shape[0])
     x_perm = gather(x, src_token)
@@ -224,6 +228,66 @@ def forward(x, w_lat, w_head, bias, w_gate, w_up, w_down, n_heads, head_dim, k,
     out = combine(y_perm, row_of, gates)
     return dict(logits=s, topk_idx=idx, gates=gates, counts=counts, offsets=offsets,
                 row_of=row_of, src_token=src_token, y_perm=y_perm, out=out)
+
+
+# ----------------------------------------------------------------------------
+# shared and modality-specific experts (36kr, section 02: shared experts carry
+# what the modalities have in common, modality-specific experts the parts
+# unique to text, picture or sound)
+# ----------------------------------------------------------------------------
+
+def modality_mask(modality, expert_ranges, E):
+    """allowed[t, e]: routed expert e lies in the range of token t's modality.
+
+    expert_ranges[m] = (begin, end) of modality m's routed experts; with no
+    ranges every expert is allowed.
+    """
+    T = len(modality)
+    if not expert_ranges:
+        return np.ones((T, E), dtype=bool)
+    allowed = np.zeros((T, E), dtype=bool)
+    for t in range(T):
+        b, e = expert_ranges[int(modality[t])]
+        allowed[t, b:e] = True
+    return allowed
+
+
+def swiglu_ffn(x, wg, wu, wd):
+    """One SwiGLU expert applied to every row: (silu(x wg^T) * (x wu^T)) wd^T."""
+    return (silu(x @ wg.T) * (x @ wu.T)) @ wd.T
+
+
+def forward_ext(x, w_lat, w_head, bias, w_gate, w_up, w_down, n_heads, head_dim, k, modality=None,
+                expert_ranges=(), n_shared=0, topk_idx=None, widen_experts=None):
+    """Layer with modality-specific routed experts and shared experts.
+
+    Routed experts are 0 .. E-1 (E = rows of w_head); a token of modality m is
+    routed only among experts [begin_m, end_m): the softmax runs over those
+    experts, the top-k is taken among them and the gates are renormalised over
+    the chosen k.  Experts E .. E+n_shared-1 of w_gate/w_up/w_down are shared:
+    every token passes through each of them with weight 1.
+        out[t] = sum_i gate[t,i] * FFN_{idx[t,i]}(x[t]) + sum_j FFN_{E+j}(x[t])
+    """
+    E = w_head.shape[0]
+    T = x.shape[0]
+    s = head_scores(latent_projection(x, w_lat), w_head, bias, n_heads, head_dim)
+    modality = np.zeros(T, dtype=np.int64) if modality is None else np.asarray(modality)
+    allowed = modality_mask(modality, expert_ranges, E)
+    s_masked = np.where(allowed, s, -np.inf)
+    p = softmax(s_masked)
+    idx = topk_select(s_masked, k) if topk_idx is None else np.asarray(topk_idx, dtype=np.int32)
+    if np.any(~np.take_along_axis(allowed, idx.astype(np.int64), 1)):
+        raise ValueError("a token was routed outside its modality's experts")
+    gates = renormalised_gates(p, idx)
+    counts, offsets, row_of, src_token = dispatch(idx, E)
+    y_perm = expert_ffn(gather(x, src_token), offsets, w_gate[:E], w_up[:E], w_down[:E], widen=widen_experts)
+    out = combine(y_perm, row_of, gates)
+    for j in range(n_shared):
+        wg, wu, wd = w_gate[E + j], w_up[E + j], w_down[E + j]
+        if widen_experts is not None:
+            wg, wu, wd = widen_experts(wg), widen_experts(wu), widen_experts(wd)
+        out = out + swiglu_ffn(x, wg, wu, wd)
+    return dict(logits=s, topk_idx=idx, gates=gates, offsets=offsets, row_of=row_of, src_token=src_token, out=out)
 
 
 def forward_bits(inp: dict, tokens=None, topk_idx=None):
@@ -235,6 +299,12 @@ def forward_bits(inp: dict, tokens=None, topk_idx=None):
     """
     cfg = inp["cfg"]
     xb = inp["x"] if tokens is None else inp["x"][np.asarray(tokens)]
+    if cfg.n_shared or cfg.modality_experts:
+        mod = inp["modality"] if tokens is None else inp["modality"][np.asarray(tokens)]
+        return forward_ext(widen_bf16(xb), widen_bf16(inp["w_lat"]), widen_bf16(inp["w_head"]), inp["bias"],
+                           inp["w_gate"], inp["w_up"], inp["w_down"], cfg.n_heads, cfg.head_dim, cfg.top_k,
+                           modality=mod, expert_ranges=cfg.modality_experts, n_shared=cfg.n_shared,
+                           topk_idx=topk_idx, widen_experts=widen_bf16)
     return forward(widen_bf16(xb), widen_bf16(inp["w_lat"]), widen_bf16(inp["w_head"]),
                    inp["bias"], inp["w_gate"], inp["w_up"], inp["w_down"],
                    cfg.n_heads, cfg.head_dim, cfg.top_k, topk_idx=topk_idx,

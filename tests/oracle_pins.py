@@ -323,3 +323,68 @@ ALL_PINS = [
     pin_silu_values, pin_single_expert_is_swiglu, pin_forward_direct, pin_subset_rows,
     pin_combine_slot_sum, pin_widen_bf16,
 ]
+
+
+# ----------------------------------------------------------------------------
+# shared and modality-specific experts
+# ----------------------------------------------------------------------------
+
+def _ext_case(g, T=30, d=8, H=2, Dh=4, E=9, I=4, S=1):
+    x = g.standard_normal((T, d))
+    w_lat, w_head = g.standard_normal((H * Dh, d)), g.standard_normal((E, H * Dh))
+    b = g.standard_normal(E)
+    wg, wu = g.standard_normal((E + S, I, d)), g.standard_normal((E + S, I, d))
+    wd = g.standard_normal((E + S, d, I))
+    return x, w_lat, w_head, b, wg, wu, wd
+
+
+def pin_ext_reduces_to_plain_layer(o):
+    """One modality covering every expert and no shared expert: the plain layer."""
+    g = np.random.default_rng(41)
+    x, w_lat, w_head, b, wg, wu, wd = _ext_case(g, S=0)
+    a = o.forward(x, w_lat, w_head, b, wg, wu, wd, 2, 4, 3)
+    e = o.forward_ext(x, w_lat, w_head, b, wg, wu, wd, 2, 4, 3, modality=np.zeros(len(x), int),
+                      expert_ranges=((0, 9),), n_shared=0)
+    np.testing.assert_array_equal(a["topk_idx"], e["topk_idx"])
+    np.testing.assert_allclose(a["out"], e["out"], rtol=1e-13, atol=1e-13)
+
+
+def pin_ext_modality_and_shared_by_definition(o):
+    """Per token, by scalar loops: only the modality's experts compete, their
+    softmax over the chosen k gives the gates, and the shared expert is added."""
+    g = np.random.default_rng(43)
+    T, k = 30, 2
+    x, w_lat, w_head, b, wg, wu, wd = _ext_case(g, T=T)
+    b[7] = 1e3                       # a huge bias on expert 7 must not leak into modality 0
+    mod = np.array([t % 3 for t in range(T)])
+    ranges = ((0, 4), (4, 7), (7, 9))
+    r = o.forward_ext(x, w_lat, w_head, b, wg, wu, wd, 2, 4, k, modality=mod, expert_ranges=ranges, n_shared=1)
+    for t in range(T):
+        lo, hi = ranges[mod[t]]
+        s = [sum(w_head[e, l] * sum(w_lat[l, i] * x[t, i] for i in range(8)) for l in range(8)) + b[e]
+             for e in range(lo, hi)]
+        order = sorted(range(hi - lo), key=lambda j: (-s[j], j))[:k]
+        assert [lo + j for j in order] == list(r["topk_idx"][t])
+        m = max(s[j] for j in order)
+        w = [math.exp(s[j] - m) for j in order]
+        acc = np.zeros(8)
+        for wi, j in zip(w, order):
+            e = lo + j
+            acc += wi / sum(w) * (wd[e] @ (_sig_vec(wg[e] @ x[t]) * (wg[e] @ x[t]) * (wu[e] @ x[t])))
+        acc += wd[9] @ (_sig_vec(wg[9] @ x[t]) * (wg[9] @ x[t]) * (wu[9] @ x[t]))
+        np.testing.assert_allclose(r["out"][t], acc, rtol=1e-10, atol=1e-10)
+
+
+def pin_ext_rejects_routing_outside_the_modality(o):
+    g = np.random.default_rng(47)
+    x, w_lat, w_head, b, wg, wu, wd = _ext_case(g, T=4)
+    try:
+        o.forward_ext(x, w_lat, w_head, b, wg, wu, wd, 2, 4, 1, modality=np.zeros(4, int),
+                      expert_ranges=((0, 3), (3, 9)), n_shared=1, topk_idx=np.array([[5], [0], [1], [2]]))
+    except ValueError:
+        return
+    raise AssertionError("routing outside the modality accepted")
+
+
+ALL_PINS += [pin_ext_reduces_to_plain_layer, pin_ext_modality_and_shared_by_definition,
+             pin_ext_rejects_routing_outside_the_modality]

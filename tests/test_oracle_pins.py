@@ -105,7 +105,16 @@ def _m_widen_shift(m):
     m.widen_bf16 = lambda b: (np.asarray(b, np.uint16).astype(np.uint32) << np.uint32(15)).view(np.float32).astype(np.float64)
 
 
-MUTANTS = [_m_bias_dropped, _m_first_head_only, _m_wlat_not_transposed, _m_ties_to_highest,
+def _m_ext_mask_ignored(m):
+    m.modality_mask = lambda modality, ranges, E: np.ones((len(modality), E), dtype=bool)
+
+
+def _m_ext_shared_gated(m):
+    f = m.swiglu_ffn
+    m.swiglu_ffn = lambda x, wg, wu, wd: 0.5 * f(x, wg, wu, wd)
+
+
+MUTANTS = [_m_ext_mask_ignored, _m_ext_shared_gated, _m_bias_dropped, _m_first_head_only, _m_wlat_not_transposed, _m_ties_to_highest,
            _m_gates_not_renormalised, _m_silu_is_sigmoid, _m_silu_on_up, _m_groups_reversed,
            _m_combine_ignores_gates, _m_softmax_wrong_axis, _m_widen_shift]
 
