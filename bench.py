@@ -257,6 +257,46 @@ def run_reference(args, rank, world):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def measure_ext_variant(torch, moe, steps: int) -> dict:
+    """moe_forward_ext on the chunk_mm workload (video|text|audio stream with
+    modality-specific routed experts and one shared expert)."""
+    cfg = mi.CONFIGS["chunk_mm"]
+    inp = mi.make_inputs(cfg)
+
+    def up(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).cuda()
+
+    n_exp = cfg.E + cfg.n_shared
+    dims = moe.moe_dims.make(cfg.T, cfg.d, cfg.E, cfg.inter, cfg.top_k, cfg.n_heads, cfg.head_dim)
+    dims_w = moe.moe_dims.make(cfg.T, cfg.d, n_exp, cfg.inter, cfg.top_k, cfg.n_heads, cfg.head_dim)
+    x, w_lat, w_head, w_down = up(inp["x"]), up(inp["w_lat"]), up(inp["w_head"]), up(inp["w_down"])
+    w13 = torch.empty((n_exp, 2 * cfg.inter, cfg.d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_prepare_weights(dims_w, up(inp["w_gate"]), up(inp["w_up"]), w13)
+    modality = torch.from_numpy(inp["modality"]).cuda()
+    ext = moe.moe_ext.make(cfg.n_shared, cfg.modality_experts, modality)
+    ws = moe.alloc_workspace(moe.moe_workspace_size_ext(dims, ext))
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        moe.moe_forward_ext(dims, ext, x, w_lat, w_head, None, w13, w_down, out, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps):
+        moe.moe_forward_ext(dims, ext, x, w_lat, w_head, None, w13, w_down, out, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status set by moe_forward_ext")
+    ms = e0.elapsed_time(e1) / steps
+    Tk = cfg.T * (cfg.top_k + cfg.n_shared)
+    flops = 2 * cfg.T * cfg.d * cfg.L + 4 * cfg.T * cfg.L * cfg.E + 6 * Tk * cfg.d * cfg.inter
+    return {"workload": workload_str(cfg) + f", experts per modality {list(cfg.modality_experts)}, "
+                                            f"{cfg.n_shared} shared expert",
+            "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "layer_tflops": flops / (ms * 1e-3) / 1e12,
+            "path": "moe_forward_ext: modality-specific routing + shared expert (extra fixed slot per token)"}
+
+
 def main():
     args = parse()
     rank, local, world = dist_env()
@@ -394,6 +434,8 @@ def main():
     if moe.moe_get_device_status(ws) != 0:
         raise SystemExit("device status set by a router variant")
 
+    ext_variant = measure_ext_variant(torch, moe, max(3, args.steps // 2)) if cfg.name == "clip" else None
+
     # end to end through the public host-buffer entry point
     e2e = None
     if not args.no_e2e:
@@ -459,6 +501,7 @@ def main():
             "router_tflops": 2 * T * (2 * d) * E / (fold_route_ms * 1e-3) / 1e12,
             "path": "moe_forward_folded: router folded to s = x (W_head W_lat)^T + b, one bf16 hi/lo GEMM "
                     "(same outputs and tolerances; h never formed)"},
+            "modality_shared_experts": ext_variant,
             "on_chip_router": {
                 "route_ms": fused_route_ms,
                 "router_tflops": alg["router_flops"] / (fused_route_ms * 1e-3) / 1e12,

@@ -29,6 +29,7 @@ MOE_ERR_TIMEOUT = -7
 MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_TIMEOUT = 0x2
 MOE_DEV_BAD_OFFSETS = 0x4
+MOE_DEV_BAD_MODALITY = 0x8
 
 
 class MoeError(RuntimeError):
@@ -50,8 +51,28 @@ class moe_dims(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class moe_ext(ctypes.Structure):
+    _fields_ = [("n_shared", ctypes.c_int32), ("n_modalities", ctypes.c_int32),
+                ("expert_begin", ctypes.c_int32 * 8), ("expert_end", ctypes.c_int32 * 8),
+                ("modality", ctypes.c_void_p)]
+
+    @classmethod
+    def make(cls, n_shared=0, ranges=(), modality=None):
+        """ranges: ((begin, end), ...) per modality; modality: device int32 [T] tensor or None."""
+        e = cls()
+        e.n_shared = int(n_shared)
+        e.n_modalities = len(ranges)
+        for m, (b, en) in enumerate(ranges):
+            e.expert_begin[m], e.expert_end[m] = int(b), int(en)
+        if modality is not None:
+            _dev(modality, dtype=torch.int32)
+            e.modality = modality.data_ptr()
+        return e
+
+
 _P = ctypes.c_void_p
 _DP = ctypes.POINTER(moe_dims)
+_XP = ctypes.POINTER(moe_ext)
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_check_dims": (ctypes.c_int, [_DP]),
@@ -76,6 +97,9 @@ _SIGS = {
     "moe_expert_gemm2": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P]),
     "moe_forward": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_workspace_size_ext": (ctypes.c_int, [_DP, _XP, ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_route_ext": (ctypes.c_int, [_DP, _XP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_ext": (ctypes.c_int, [_DP, _XP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_host": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
@@ -292,6 +316,30 @@ def moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws, stream=None)
     _dev(bias, dtype=torch.float32)
     _check(lib().moe_forward(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(w13),
                              _ptr(w_down), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+
+
+def moe_workspace_size_ext(dims, ext) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_ext(ctypes.byref(dims), ctypes.byref(ext), ctypes.byref(n)),
+           "moe_workspace_size_ext")
+    return n.value
+
+
+def moe_route_ext(dims, ext, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _dev(x, w_lat, w_head, dtype=torch.bfloat16)
+    _dev(bias, topk_gate, logits, dtype=torch.float32)
+    _dev(topk_idx, dtype=torch.int32)
+    _check(lib().moe_route_ext(ctypes.byref(dims), ctypes.byref(ext), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias),
+                               _ptr(topk_idx), _ptr(topk_gate), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_route_ext")
+
+
+def moe_forward_ext(dims, ext, x, w_lat, w_head, bias, w13, w_down, out, ws, stream=None) -> None:
+    _dev(x, w_lat, w_head, w13, w_down, out, dtype=torch.bfloat16)
+    _dev(bias, dtype=torch.float32)
+    _check(lib().moe_forward_ext(ctypes.byref(dims), ctypes.byref(ext), _ptr(x), _ptr(w_lat), _ptr(w_head),
+                                 _ptr(bias), _ptr(w13), _ptr(w_down), _ptr(out), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "moe_forward_ext")
 
 
 def moe_forward_host(dims, x_host, w_lat, w_head, bias, w13, w_down, out_host, ws, stream=None) -> None:

@@ -180,14 +180,87 @@ struct EpiHiLo {
 // -> + bias -> optional logits row -> top-k (value descending, ties to the
 // lower expert index) -> softmax over the chosen k -> idx/gate rows.  All 32
 // lanes of the warp must call it (the TMEM loads are warp-collective).
+constexpr int kMaxModalities = 8;
+
 struct TopKParams {
   const float* bias;  // [E] or nullptr
   float* logits;      // [T, E] or nullptr
-  int32_t* idx;       // [T, k]
-  float* gate;        // [T, k]
+  int32_t* idx;       // [T, k_out]
+  float* gate;        // [T, k_out]
   int E;
   int k;
+  // Modality-specific routing and shared experts (all zero/null: plain layer).
+  int k_out;                     // row stride of idx/gate: k + n_shared (0 means k)
+  int n_shared;                  // slots k .. k_out-1 get experts E .. E+n_shared-1, gate 1
+  const int32_t* modality;       // [T] modality id, or nullptr: every expert competes
+  int n_mod;
+  int ebeg[kMaxModalities], eend[kMaxModalities];
+  int* status;                   // MOE_DEV_BAD_MODALITY for an id outside [0, n_mod)
 };
+
+inline TopKParams make_topk_params(const RouteArgs& a) {
+  TopKParams p{};
+  p.bias = a.bias;
+  p.logits = a.logits;
+  p.idx = a.topk_idx;
+  p.gate = a.topk_gate;
+  p.E = a.E;
+  p.k = a.k;
+  p.k_out = a.k + a.ext.n_shared;
+  p.n_shared = a.ext.n_shared;
+  p.modality = a.ext.n_mod > 0 ? a.ext.modality : nullptr;
+  p.n_mod = a.ext.n_mod;
+  for (int m = 0; m < kMaxModalities; ++m) {
+    p.ebeg[m] = a.ext.ebeg[m];
+    p.eend[m] = a.ext.eend[m];
+  }
+  p.status = a.status;
+  return p;
+}
+
+// The routed experts token `row` may choose: [*lo, *hi).
+__device__ __forceinline__ void expert_range(const TopKParams& p, int row, bool valid, int* lo, int* hi) {
+  *lo = 0;
+  *hi = p.E;
+  if (p.modality != nullptr && valid) {
+    const int m = __ldg(p.modality + row);
+    if (m >= 0 && m < p.n_mod) {
+      *lo = p.ebeg[m];
+      *hi = p.eend[m];
+    } else {
+      *hi = 0;  // no candidates: the row's routed slots get id -1
+      if (p.status != nullptr) atomicOr(p.status, MOE_DEV_BAD_MODALITY);
+    }
+  }
+}
+
+// Writes the k chosen experts (bi, bv; value-ordered) and the shared slots.
+__device__ __forceinline__ void write_topk(const TopKParams& p, int row, const float (&bv)[kMaxTopK],
+                                           const int (&bi)[kMaxTopK]) {
+  const float m = bv[0];
+  float w[kMaxTopK];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxTopK; ++i) {
+    w[i] = (i < p.k && bi[i] >= 0) ? expf(bv[i] - m) : 0.f;
+    sum += w[i];
+  }
+  const float inv = sum > 0.f ? 1.0f / sum : 0.f;
+  const int ko = p.k_out > 0 ? p.k_out : p.k;
+  int32_t* io = p.idx + static_cast<int64_t>(row) * ko;
+  float* go = p.gate + static_cast<int64_t>(row) * ko;
+#pragma unroll
+  for (int i = 0; i < kMaxTopK; ++i) {
+    if (i < p.k) {
+      io[i] = bi[i];
+      go[i] = w[i] * inv;
+    }
+  }
+  for (int j = 0; j < p.n_shared; ++j) {
+    io[p.k + j] = p.E + j;
+    go[p.k + j] = 1.0f;
+  }
+}
 
 template <int BN>
 __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, int row, bool valid) {
@@ -195,6 +268,8 @@ __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, in
   int bi[kMaxTopK];
 #pragma unroll
   for (int i = 0; i < kMaxTopK; ++i) { bv[i] = -INFINITY; bi[i] = -1; }
+  int e_lo, e_hi;
+  expert_range(p, row, valid, &e_lo, &e_hi);
   float* lrow = (p.logits != nullptr && valid) ? p.logits + static_cast<int64_t>(row) * p.E : nullptr;
 #pragma unroll 1
   for (int col = 0; col < BN; col += 16) {
@@ -209,7 +284,7 @@ __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, in
         float s = __uint_as_float(u[j]);
         if (p.bias != nullptr) s += __ldg(p.bias + e);
         if (lrow != nullptr) lrow[e] = s;
-        if (s > bv[kMaxTopK - 1]) {
+        if (e >= e_lo && e < e_hi && s > bv[kMaxTopK - 1]) {
           float cv = s;
           int ci = e;
 #pragma unroll
@@ -227,24 +302,7 @@ __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, in
     }
   }
   if (!valid) return;
-  const float m = bv[0];
-  float w[kMaxTopK];
-  float sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxTopK; ++i) {
-    w[i] = (i < p.k) ? expf(bv[i] - m) : 0.f;
-    sum += w[i];
-  }
-  const float inv = 1.0f / sum;
-  int32_t* io = p.idx + static_cast<int64_t>(row) * p.k;
-  float* go = p.gate + static_cast<int64_t>(row) * p.k;
-#pragma unroll
-  for (int i = 0; i < kMaxTopK; ++i) {
-    if (i < p.k) {
-      io[i] = bi[i];
-      go[i] = w[i] * inv;
-    }
-  }
+  write_topk(p, row, bv, bi);
 }
 
 // Router stage 2: summed head scores (fp32 accumulator, all E experts in one

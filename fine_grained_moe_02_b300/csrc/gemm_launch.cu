@@ -107,7 +107,7 @@ int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream) {
     if (!make_tmap_bf16_2d(&ta, a.hl, 2ULL * a.L, a.T, kBK, kBM)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16_2d(&tb, a.w_head, a.L, a.E, kBK, bn)) return MOE_ERR_CUDA;
     GemmShape sh{2 * a.L, a.L, bn, 1, nullptr, static_cast<int>(a.T), a.status};
-    EpiTopK::Params ep{a.bias, a.logits, a.topk_idx, a.topk_gate, a.E, a.k};
+    EpiTopK::Params ep = make_topk_params(a);
     const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
     return run_gemm_bn<EpiTopK>(bn, ta, tb, ta /* no bulk output */, sh, ep, grid, stream);
   }
@@ -122,7 +122,7 @@ int launch_route_folded(const RouteArgs& a, const uint16_t* w_router, cudaStream
   if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, kBM)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&tb, w_router, 2ULL * a.d, a.E, kBK, bn)) return MOE_ERR_CUDA;
   GemmShape sh{2 * a.d, 2 * a.d, bn, 1, nullptr, static_cast<int>(a.T), a.status, nullptr, a.d};
-  EpiTopK::Params ep{a.bias, a.logits, a.topk_idx, a.topk_gate, a.E, a.k};
+  EpiTopK::Params ep = make_topk_params(a);
   const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
   return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream);
 }

@@ -25,6 +25,14 @@ struct DispatchArgs {
   int sm_count;
 };
 
+// Modality-specific routing and shared experts (zero-initialised: plain layer).
+struct RouteExt {
+  int n_shared;
+  int n_mod;
+  int ebeg[8], eend[8];
+  const int32_t* modality;
+};
+
 struct RouteArgs {
   const uint16_t* x;
   const uint16_t* w_lat;
@@ -38,6 +46,7 @@ struct RouteArgs {
   int64_t T;
   int d, L, E, k;
   int head_dim;
+  RouteExt ext;
   int* status;
   int sm_count;
 };

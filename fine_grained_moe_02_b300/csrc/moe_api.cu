@@ -509,6 +509,122 @@ int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* 
   return moe_combine(dims, xperm, row_of, gate, out, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+int check_ext(const moe_dims* d, const moe_ext* x) {
+  if (x == nullptr) return MOE_ERR_INVALID_ARG;
+  if (x->n_shared < 0 || x->n_modalities < 0 || x->n_modalities > 8) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->top_k + x->n_shared > kMaxTopK || d->E + x->n_shared > kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  for (int m = 0; m < x->n_modalities; ++m) {
+    const int b = x->expert_begin[m], e = x->expert_end[m];
+    if (b < 0 || e > d->E || e - b < d->top_k) return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (x->modality != nullptr && (reinterpret_cast<uintptr_t>(x->modality) & 3u)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+moe_dims expanded(const moe_dims* d, const moe_ext* x) {
+  moe_dims e = *d;
+  e.E += x->n_shared;
+  e.top_k += x->n_shared;
+  return e;
+}
+
+RouteExt route_ext_of(const moe_ext* x) {
+  RouteExt r{};
+  r.n_shared = x->n_shared;
+  r.n_mod = x->modality != nullptr ? x->n_modalities : 0;
+  for (int m = 0; m < 8; ++m) {
+    r.ebeg[m] = m < x->n_modalities ? x->expert_begin[m] : 0;
+    r.eend[m] = m < x->n_modalities ? x->expert_end[m] : 0;
+  }
+  r.modality = x->modality;
+  return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_workspace_size_ext(const moe_dims* dims, const moe_ext* ext, size_t* bytes) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_ext(dims, ext)) != MOE_OK) return rc;
+  const moe_dims d2 = expanded(dims, ext);
+  return moe_workspace_size(&d2, bytes);
+}
+
+int moe_route_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x, const moe_bf16* w_lat,
+                  const moe_bf16* w_head, const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
+                  void* ws, size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_ext(dims, ext)) != MOE_OK) return rc;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || topk_idx == nullptr || topk_gate == nullptr ||
+      ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(topk_idx) || !aligned16(topk_gate) ||
+      !aligned16(ws) || (bias != nullptr && !aligned16(bias)) || (logits != nullptr && !aligned16(logits)))
+    return MOE_ERR_MISALIGNED;
+  const ScratchLayout sl = scratch_layout(dims);
+  if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  RouteArgs a{};
+  a.x = x;
+  a.w_lat = w_lat;
+  a.w_head = w_head;
+  a.bias = bias;
+  a.topk_idx = topk_idx;
+  a.topk_gate = topk_gate;
+  a.logits = logits;
+  a.hl = at<uint16_t>(ws, sl.hl);
+  a.T = dims->T;
+  a.d = dims->d;
+  a.L = dims->n_heads * dims->head_dim;
+  a.E = dims->E;
+  a.k = dims->top_k;
+  a.head_dim = dims->head_dim;
+  a.ext = route_ext_of(ext);
+  a.status = status_ptr(ws);
+  a.sm_count = sms;
+  return launch_route(a, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x, const moe_bf16* w_lat,
+                    const moe_bf16* w_head, const float* bias, const moe_bf16* w13, const moe_bf16* w_down,
+                    moe_bf16* out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_ext(dims, ext)) != MOE_OK) return rc;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
+      out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(w13) || !aligned16(w_down) ||
+      !aligned16(out) || !aligned16(ws) || (bias != nullptr && !aligned16(bias)))
+    return MOE_ERR_MISALIGNED;
+  const moe_dims d2 = expanded(dims, ext);
+  if ((rc = moe_check_dims(&d2)) != MOE_OK) return rc;
+  const ForwardLayout f = forward_layout(&d2);
+  if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
+  int32_t* idx = at<int32_t>(ws, f.idx);
+  float* gate = at<float>(ws, f.gate);
+  int32_t* offsets = at<int32_t>(ws, f.offsets);
+  int32_t* row_of = at<int32_t>(ws, f.row_of);
+  int32_t* src = at<int32_t>(ws, f.src);
+  moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
+  moe_bf16* act = at<moe_bf16>(ws, f.act);
+  if ((rc = moe_route_ext(dims, ext, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK)
+    return rc;
+  if ((rc = moe_dispatch(&d2, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm1(&d2, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm2(&d2, act, offsets, w_down, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  return moe_combine(&d2, xperm, row_of, gate, out, stream);
+}
+
 int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* w_lat, const moe_bf16* w_head,
                      const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out_host, void* ws,
                      size_t ws_bytes, void* stream) {

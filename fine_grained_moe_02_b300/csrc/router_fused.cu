@@ -318,6 +318,8 @@ __global__ void __launch_bounds__(256) topk_combine_kernel(const float* __restri
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t t = wid; t < T; t += nw) {
+    int e_lo, e_hi;
+    expert_range(p, static_cast<int>(t), true, &e_lo, &e_hi);
     float v[kMaxExperts / 32];
 #pragma unroll
     for (int j = 0; j < kMaxExperts / 32; ++j) {
@@ -329,10 +331,12 @@ __global__ void __launch_bounds__(256) topk_combine_kernel(const float* __restri
         if (p.bias != nullptr) s += __ldg(p.bias + e);
         if (p.logits != nullptr) p.logits[t * E + e] = s;
       }
-      v[j] = s;
+      v[j] = (e >= e_lo && e < e_hi) ? s : -INFINITY;
     }
     float sel_v[kMaxTopK];
     int sel_e[kMaxTopK];
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i) { sel_v[i] = -INFINITY; sel_e[i] = -1; }
 #pragma unroll
     for (int i = 0; i < kMaxTopK; ++i) {
       if (i >= p.k) break;
@@ -350,27 +354,12 @@ __global__ void __launch_bounds__(256) topk_combine_kernel(const float* __restri
         if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
       }
       sel_v[i] = bv;
-      sel_e[i] = be;
+      sel_e[i] = (be < E && bv > -INFINITY) ? be : -1;
 #pragma unroll
       for (int j = 0; j < kMaxExperts / 32; ++j)
         if (lane + 32 * j == be) v[j] = -INFINITY;
     }
-    if (lane == 0) {
-      float w[kMaxTopK], sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxTopK; ++i) {
-        w[i] = (i < p.k) ? expf(sel_v[i] - sel_v[0]) : 0.f;
-        sum += w[i];
-      }
-      const float inv = 1.0f / sum;
-#pragma unroll
-      for (int i = 0; i < kMaxTopK; ++i) {
-        if (i < p.k) {
-          p.idx[t * p.k + i] = sel_e[i] < E ? sel_e[i] : -1;
-          p.gate[t * p.k + i] = w[i] * inv;
-        }
-      }
-    }
+    if (lane == 0) write_topk(p, static_cast<int>(t), sel_v, sel_e);
   }
 }
 
@@ -386,7 +375,7 @@ int run_fused(const RouteArgs& a, int head_dim, cudaStream_t stream) {
   fa.head_dim = head_dim;
   fa.n_heads = a.L / head_dim;
   fa.E = a.E;
-  fa.tp = TopKParams{a.bias, a.logits, a.topk_idx, a.topk_gate, a.E, a.k};
+  fa.tp = make_topk_params(a);
   fa.status = a.status;
   fa.wait_ns = kWaitLimitNs;
   // Head groups per token tile (G | n_heads).  Every tile re-reads its x slice

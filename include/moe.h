@@ -83,6 +83,7 @@ typedef enum moe_status {
 #define MOE_DEV_BAD_EXPERT_ID 0x1  /* topk_idx held an id outside [0, E); that slot was skipped */
 #define MOE_DEV_TIMEOUT 0x2        /* a pipeline wait exceeded its limit; that kernel stopped early */
 #define MOE_DEV_BAD_OFFSETS 0x4    /* group offsets not monotone / out of range; no tile was run */
+#define MOE_DEV_BAD_MODALITY 0x8   /* a token's modality id is outside [0, n_modalities); its routed slots are -1 */
 
 /* Human-readable name of a moe_status value.  Never NULL. */
 const char* moe_status_string(int status);
@@ -272,6 +273,47 @@ int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, 
 int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
                        const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws, size_t ws_bytes,
                        void* stream);
+
+/* Shared and modality-specific experts (36kr article, section 02: shared
+ * experts carry what the modalities have in common, modality-specific
+ * experts what is unique to language, picture or sound).  The E routed
+ * experts are split into per-modality ranges [expert_begin[m], expert_end[m]);
+ * a token of modality m is routed only within its range (softmax, top-k and
+ * renormalised gates over those experts).  n_shared shared experts, stored
+ * after the routed ones in w13/w_down (ids E .. E+n_shared-1), process every
+ * token with weight 1:
+ *   out[t] = sum_i gate[t,i] FFN_{idx[t,i]}(x[t]) + sum_j FFN_{E+j}(x[t])
+ * Rules: n_shared >= 0, top_k + n_shared <= 8, E + n_shared <= 256,
+ * 0 <= n_modalities <= 8 (0: no masking), each range inside [0, E) with at
+ * least top_k experts.  modality: device int32 [T] (4-byte aligned), or NULL
+ * for no masking; an id outside [0, n_modalities) sets MOE_DEV_BAD_MODALITY
+ * and leaves that token's routed slots at -1. */
+typedef struct moe_ext {
+  int32_t n_shared;
+  int32_t n_modalities;
+  int32_t expert_begin[8];
+  int32_t expert_end[8];
+  const int32_t* modality;
+} moe_ext;
+
+/* Workspace for moe_forward_ext (= moe_workspace_size with E + n_shared
+ * experts and top_k + n_shared slots). */
+int moe_workspace_size_ext(const moe_dims* dims, const moe_ext* ext, size_t* bytes);
+
+/* Routing with modality ranges; writes top_k + n_shared slots per token
+ * (topk_idx/topk_gate [T, top_k + n_shared]: the routed slots, then the
+ * shared experts with gate 1).  logits [T, E] (optional) are the unmasked
+ * summed scores.  Other arguments as in moe_route. */
+int moe_route_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x, const moe_bf16* w_lat,
+                  const moe_bf16* w_head, const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer with modality ranges and shared experts.  w13
+ * [E + n_shared, 2*inter, d] (moe_prepare_weights with E + n_shared experts),
+ * w_down [E + n_shared, d, inter]; ws: moe_workspace_size_ext bytes. */
+int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x, const moe_bf16* w_lat,
+                    const moe_bf16* w_head, const float* bias, const moe_bf16* w13, const moe_bf16* w_down,
+                    moe_bf16* out, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward for a caller whose activations live in host memory: copies
  * x_host [T, d] to the device, runs the layer, copies out to out_host [T, d]

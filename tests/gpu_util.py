@@ -57,10 +57,16 @@ class Dev:
         self.bias = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).cuda()
         self.w_down = dev_bf16(inp["w_down"])
         wg, wu = dev_bf16(inp["w_gate"]), dev_bf16(inp["w_up"])
-        self.w13 = torch.empty((cfg.E, 2 * cfg.inter, cfg.d), dtype=torch.bfloat16, device="cuda")
-        moe.moe_prepare_weights(self.dims, wg, wu, self.w13)
+        n_exp = wg.shape[0]                      # routed + shared experts
+        self.w13 = torch.empty((n_exp, 2 * cfg.inter, cfg.d), dtype=torch.bfloat16, device="cuda")
+        dims_w = moe.moe_dims.make(cfg.T, cfg.d, n_exp, cfg.inter, min(cfg.top_k, n_exp), cfg.n_heads, cfg.head_dim)
+        moe.moe_prepare_weights(dims_w, wg, wu, self.w13)
         del wg, wu
-        self.ws = moe.alloc_workspace(moe.moe_workspace_size(self.dims))
+        self.modality = torch.from_numpy(inp["modality"]).cuda() if "modality" in inp else None
+        self.ext = moe.moe_ext.make(cfg.n_shared, cfg.modality_experts,
+                                    self.modality if cfg.modality_experts else None)
+        self.ws = moe.alloc_workspace(max(moe.moe_workspace_size(self.dims),
+                                          moe.moe_workspace_size_ext(self.dims, self.ext)))
 
     # -- stages
     def route(self, want_logits=True):
@@ -104,6 +110,22 @@ class Dev:
         out = torch.empty((self.cfg.T, self.cfg.d), dtype=torch.bfloat16, device="cuda")
         moe.moe_forward(self.dims, self.x, self.w_lat, self.w_head, self.bias, self.w13, self.w_down, out, self.ws)
         return out
+
+    def forward_ext(self):
+        out = torch.empty((self.cfg.T, self.cfg.d), dtype=torch.bfloat16, device="cuda")
+        moe.moe_forward_ext(self.dims, self.ext, self.x, self.w_lat, self.w_head, self.bias, self.w13, self.w_down,
+                            out, self.ws)
+        return out
+
+    def route_ext(self):
+        T, k, E = self.cfg.T, self.cfg.top_k, self.cfg.E
+        ko = k + self.cfg.n_shared
+        idx = torch.empty((T, ko), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, ko), dtype=torch.float32, device="cuda")
+        logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        moe.moe_route_ext(self.dims, self.ext, self.x, self.w_lat, self.w_head, self.bias, idx, gate, logits,
+                          self.ws)
+        return idx, gate, logits
 
     def status(self) -> int:
         return moe.moe_get_device_status(self.ws)
@@ -169,3 +191,20 @@ def check_out(out_gpu: np.ndarray, out_ref: np.ndarray) -> dict:
 def small_inputs(name="edge", seed=0, **kw):
     cfg = mi.custom_config(name, seed=seed, **kw)
     return mi.make_inputs(cfg)
+
+
+def check_routing_ext(inp, s_ref, idx_gpu, gate_gpu, logits_gpu=None, tokens=None):
+    """Routing parity with modality ranges and shared slots: the routed slots
+    against the oracle's masked scores, then the shared slots."""
+    cfg = inp["cfg"]
+    k, S, E = cfg.top_k, cfg.n_shared, cfg.E
+    mod = inp["modality"] if tokens is None else inp["modality"][tokens]
+    allowed = O.modality_mask(mod, cfg.modality_experts, E)
+    if logits_gpu is not None:
+        err = np.abs(logits_gpu.astype(np.float64) - s_ref).max()
+        assert err <= LOGIT_TOL, f"logit max-abs {err}"
+    s_masked = np.where(allowed, s_ref, -np.inf)
+    check_routing(s_masked, idx_gpu[:, :k], gate_gpu[:, :k], k)
+    assert np.all(np.take_along_axis(allowed, idx_gpu[:, :k].astype(np.int64), 1))
+    for j in range(S):
+        assert np.all(idx_gpu[:, k + j] == E + j) and np.all(gate_gpu[:, k + j] == 1.0)
