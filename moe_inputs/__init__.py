@@ -48,6 +48,7 @@ class MoeConfig:
     modality_split: tuple = ()       # ((n_tokens, x_scale), ...) in sequence order
     modality_experts: tuple = ()     # ((begin, end), ...) routed experts of each modality; () = no masking
     n_shared: int = 0                # shared experts, stored after the E routed experts
+    head_local: bool = False         # head-local MoE: d = n_heads*head_dim split into heads, E experts per head
     seed: int = 0
     note: str = ""
 
@@ -83,12 +84,18 @@ CONFIGS = {
                           modality_experts=((0, 96), (96, 112), (112, 128)), n_shared=1,
                           note="24-frame chunk with modality-specific experts (video 96, text 16, audio 16) "
                                "and one shared expert"),
+    # head-local MultiHead MoE: 3072 = 12 x 256 split into heads, 256 experts
+    # per head, top-6 per head (72 experts per token), head-local experts
+    # 256 -> 512 -> 256; one 24-frame chunk of video tokens
+    "headlocal": MoeConfig("headlocal", T=10752, d=3072, E=256, inter=512, head_local=True,
+                           note="head-local MoE: 12 heads x 256 dims, 256 experts per head, top-6 per head, "
+                                "expert inter 512, T=10752"),
     # not one of the pages' workloads: a 4096-token slice at clip width with 32
     # experts, small enough (~1.5 GB on the device) for full profiler captures
     "slice": MoeConfig("slice", T=4096, d=4096, E=32, inter=1024,
                        note="profiling size: 4096 tokens, d=4096, E=32, inter=1024"),
 }
-CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "slice"]
+CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "headlocal", "slice"]
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -244,6 +251,16 @@ def make_weights(cfg: MoeConfig) -> dict:
     w_lat [L, d], w_head [E, L], w_gate/w_up [E, inter, d], w_down [E, d, inter],
     bias [E] float32 or None.
     """
+    if cfg.head_local:
+        H, Dh = cfg.n_heads, cfg.head_dim
+        assert cfg.d == H * Dh
+        return dict(
+            w_router=_w(cfg, "w_head", (H, cfg.E, Dh), Dh, True),
+            w_gate=_w(cfg, "w_gate", (H, cfg.E, cfg.inter, Dh), Dh, False),
+            w_up=_w(cfg, "w_up", (H, cfg.E, cfg.inter, Dh), Dh, False),
+            w_down=_w(cfg, "w_down", (H, cfg.E, Dh, cfg.inter), cfg.inter, False),
+            bias=None,
+        )
     n_exp = cfg.E + cfg.n_shared   # shared experts follow the routed ones
     return dict(
         w_lat=_w(cfg, "w_lat", (cfg.L, cfg.d), cfg.d, True),

@@ -290,6 +290,46 @@ def forward_ext(x, w_lat, w_head, bias, w_gate, w_up, w_down, n_heads, head_dim,
     return dict(logits=s, topk_idx=idx, gates=gates, offsets=offsets, row_of=row_of, src_token=src_token, out=out)
 
 
+# ----------------------------------------------------------------------------
+# head-local MultiHead MoE (36kr, section 02: the hidden representation split
+# into heads, each head choosing its own experts in its own subspace, the
+# head results fused again)
+# ----------------------------------------------------------------------------
+
+def forward_headlocal(x, w_router, bias, w_gate, w_up, w_down, n_heads, head_dim, k, topk_idx=None,
+                      widen_experts=None):
+    """Head-local MoE: x [T, n_heads*head_dim] is split into head slices
+    x_j = x[:, j*head_dim:(j+1)*head_dim]; head j scores its own experts,
+    s_j = x_j W_router[j]^T + b[j] ([E_h] per head), takes the softmax, the
+    top-k (ties to the lowest index) and renormalised gates, runs the chosen
+    head-local SwiGLU experts (head_dim -> inter -> head_dim, weights
+    w_gate/w_up [H, E_h, inter, head_dim], w_down [H, E_h, head_dim, inter])
+    and the head outputs are concatenated back into out [T, n_heads*head_dim].
+    topk_idx [H, T, k] (optional) fixes the routing decision.
+    """
+    T = x.shape[0]
+    out = np.zeros((T, n_heads * head_dim), dtype=np.float64)
+    idx_all, gates_all, logits_all = [], [], []
+    for j in range(n_heads):
+        cols = slice(j * head_dim, (j + 1) * head_dim)
+        xj = x[:, cols]
+        wr = w_router[j] if widen_experts is None else widen_experts(w_router[j])
+        s = xj @ wr.T
+        if bias is not None:
+            s = s + np.asarray(bias[j], dtype=np.float64)[None, :]
+        p = softmax(s)
+        idx = topk_select(s, k) if topk_idx is None else np.asarray(topk_idx[j], dtype=np.int32)
+        gates = renormalised_gates(p, idx)
+        E_h = wr.shape[0]
+        _, offsets, row_of, src_token = dispatch(idx, E_h)
+        y_perm = expert_ffn(gather(xj, src_token), offsets, w_gate[j], w_up[j], w_down[j], widen=widen_experts)
+        out[:, cols] = combine(y_perm, row_of, gates)
+        idx_all.append(idx)
+        gates_all.append(gates)
+        logits_all.append(s)
+    return dict(out=out, topk_idx=np.stack(idx_all), gates=np.stack(gates_all), logits=np.stack(logits_all))
+
+
 def forward_bits(inp: dict, tokens=None, topk_idx=None):
     """Convenience: run ``forward`` on the bf16-bit input dict of moe_inputs.
 
@@ -299,6 +339,10 @@ def forward_bits(inp: dict, tokens=None, topk_idx=None):
     """
     cfg = inp["cfg"]
     xb = inp["x"] if tokens is None else inp["x"][np.asarray(tokens)]
+    if cfg.head_local:
+        return forward_headlocal(widen_bf16(xb), inp["w_router"], inp["bias"], inp["w_gate"], inp["w_up"],
+                                 inp["w_down"], cfg.n_heads, cfg.head_dim, cfg.top_k, topk_idx=topk_idx,
+                                 widen_experts=widen_bf16)
     if cfg.n_shared or cfg.modality_experts:
         mod = inp["modality"] if tokens is None else inp["modality"][np.asarray(tokens)]
         return forward_ext(widen_bf16(xb), widen_bf16(inp["w_lat"]), widen_bf16(inp["w_head"]), inp["bias"],

@@ -388,3 +388,54 @@ def pin_ext_rejects_routing_outside_the_modality(o):
 
 ALL_PINS += [pin_ext_reduces_to_plain_layer, pin_ext_modality_and_shared_by_definition,
              pin_ext_rejects_routing_outside_the_modality]
+
+
+# ----------------------------------------------------------------------------
+# head-local MultiHead MoE
+# ----------------------------------------------------------------------------
+
+def _hl_case(g, T=20, H=3, Dh=4, E=5, I=3):
+    x = g.standard_normal((T, H * Dh))
+    wr = g.standard_normal((H, E, Dh))
+    b = g.standard_normal((H, E))
+    wg, wu = g.standard_normal((H, E, I, Dh)), g.standard_normal((H, E, I, Dh))
+    wd = g.standard_normal((H, E, Dh, I))
+    return x, wr, b, wg, wu, wd
+
+
+def pin_headlocal_by_definition(o):
+    """Per token and head, by scalar loops: the head's own slice scores its
+    own experts; the k best (ties to the lowest index) are gated by their
+    softmax; the head's slot of the output is their gate-weighted sum."""
+    g = np.random.default_rng(51)
+    T, H, Dh, E, k = 20, 3, 4, 5, 2
+    x, wr, b, wg, wu, wd = _hl_case(g)
+    r = o.forward_headlocal(x, wr, b, wg, wu, wd, H, Dh, k)
+    for t in range(T):
+        for j in range(H):
+            xj = x[t, j * Dh:(j + 1) * Dh]
+            s = [sum(wr[j, e, i] * xj[i] for i in range(Dh)) + b[j, e] for e in range(E)]
+            order = sorted(range(E), key=lambda e: (-s[e], e))[:k]
+            assert list(r["topk_idx"][j, t]) == order
+            w = [math.exp(s[e] - s[order[0]]) for e in order]
+            acc = np.zeros(Dh)
+            for wi, e in zip(w, order):
+                gg, uu = wg[j, e] @ xj, wu[j, e] @ xj
+                acc += wi / sum(w) * (wd[j, e] @ (gg * _sig_vec(gg) * uu))
+            np.testing.assert_allclose(r["out"][t, j * Dh:(j + 1) * Dh], acc, rtol=1e-11, atol=1e-11)
+
+
+def pin_headlocal_heads_are_independent(o):
+    """Changing one head's slice changes only that head's output columns."""
+    g = np.random.default_rng(53)
+    x, wr, b, wg, wu, wd = _hl_case(g)
+    r1 = o.forward_headlocal(x, wr, b, wg, wu, wd, 3, 4, 2)
+    x2 = x.copy()
+    x2[:, 4:8] += g.standard_normal((x.shape[0], 4))
+    r2 = o.forward_headlocal(x2, wr, b, wg, wu, wd, 3, 4, 2)
+    np.testing.assert_array_equal(r1["out"][:, :4], r2["out"][:, :4])
+    np.testing.assert_array_equal(r1["out"][:, 8:], r2["out"][:, 8:])
+    assert np.abs(r1["out"][:, 4:8] - r2["out"][:, 4:8]).max() > 1e-6
+
+
+ALL_PINS += [pin_headlocal_by_definition, pin_headlocal_heads_are_independent]

@@ -114,7 +114,15 @@ def _m_ext_shared_gated(m):
     m.swiglu_ffn = lambda x, wg, wu, wd: 0.5 * f(x, wg, wu, wd)
 
 
-MUTANTS = [_m_ext_mask_ignored, _m_ext_shared_gated, _m_bias_dropped, _m_first_head_only, _m_wlat_not_transposed, _m_ties_to_highest,
+def _m_headlocal_wrong_slice(m):
+    f = m.forward_headlocal
+
+    def hl(x, w_router, bias, w_gate, w_up, w_down, n_heads, head_dim, k, **kw):
+        return f(np.roll(x, head_dim, axis=1), w_router, bias, w_gate, w_up, w_down, n_heads, head_dim, k, **kw)
+    m.forward_headlocal = hl
+
+
+MUTANTS = [_m_headlocal_wrong_slice, _m_ext_mask_ignored, _m_ext_shared_gated, _m_bias_dropped, _m_first_head_only, _m_wlat_not_transposed, _m_ties_to_highest,
            _m_gates_not_renormalised, _m_silu_is_sigmoid, _m_silu_on_up, _m_groups_reversed,
            _m_combine_ignores_gates, _m_softmax_wrong_axis, _m_widen_shift]
 
