@@ -257,6 +257,40 @@ def run_reference(args, rank, world):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def measure_headlocal_variant(torch, moe, steps: int) -> dict:
+    """moe_forward_headlocal on the headlocal workload (12 x 256 head slices,
+    256 experts per head, top-6 per head)."""
+    cfg = mi.CONFIGS["headlocal"]
+    inp = mi.make_inputs(cfg)
+
+    def up(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).cuda()
+
+    dims = moe.moe_dims.make(cfg.T, cfg.d, cfg.E, cfg.inter, cfg.top_k, cfg.n_heads, cfg.head_dim)
+    x, w_router, w_down = up(inp["x"]), up(inp["w_router"]), up(inp["w_down"])
+    w13 = torch.empty((cfg.n_heads, cfg.E, 2 * cfg.inter, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+    moe.moe_prepare_weights_headlocal(dims, up(inp["w_gate"]), up(inp["w_up"]), w13)
+    ws = moe.alloc_workspace(moe.moe_workspace_size_headlocal(dims))
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        moe.moe_forward_headlocal(dims, x, w_router, None, w13, w_down, out, None, None, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(steps):
+        moe.moe_forward_headlocal(dims, x, w_router, None, w13, w_down, out, None, None, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status set by moe_forward_headlocal")
+    ms = e0.elapsed_time(e1) / steps
+    flops = cfg.T * cfg.n_heads * (2 * cfg.head_dim * cfg.E + 6 * cfg.top_k * cfg.head_dim * cfg.inter)
+    return {"workload": cfg.note, "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "layer_tflops": flops / (ms * 1e-3) / 1e12,
+            "path": "moe_forward_headlocal: per head, router GEMM + top-k, sort, grouped SwiGLU GEMMs, combine "
+                    "into the head's columns; heads in sequence on one stream"}
+
+
 def measure_ext_variant(torch, moe, steps: int) -> dict:
     """moe_forward_ext on the chunk_mm workload (video|text|audio stream with
     modality-specific routed experts and one shared expert)."""
@@ -435,6 +469,7 @@ def main():
         raise SystemExit("device status set by a router variant")
 
     ext_variant = measure_ext_variant(torch, moe, max(3, args.steps // 2)) if cfg.name == "clip" else None
+    hl_variant = measure_headlocal_variant(torch, moe, max(3, args.steps // 2)) if cfg.name == "clip" else None
 
     # end to end through the public host-buffer entry point
     e2e = None
@@ -502,6 +537,7 @@ def main():
             "path": "moe_forward_folded: router folded to s = x (W_head W_lat)^T + b, one bf16 hi/lo GEMM "
                     "(same outputs and tolerances; h never formed)"},
             "modality_shared_experts": ext_variant,
+            "head_local_moe": hl_variant,
             "on_chip_router": {
                 "route_ms": fused_route_ms,
                 "router_tflops": alg["router_flops"] / (fused_route_ms * 1e-3) / 1e12,

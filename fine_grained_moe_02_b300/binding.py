@@ -100,6 +100,9 @@ _SIGS = {
     "moe_workspace_size_ext": (ctypes.c_int, [_DP, _XP, ctypes.POINTER(ctypes.c_size_t)]),
     "moe_route_ext": (ctypes.c_int, [_DP, _XP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_ext": (ctypes.c_int, [_DP, _XP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_workspace_size_headlocal": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_prepare_weights_headlocal": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
+    "moe_forward_headlocal": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_host": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
@@ -340,6 +343,27 @@ def moe_forward_ext(dims, ext, x, w_lat, w_head, bias, w13, w_down, out, ws, str
     _check(lib().moe_forward_ext(ctypes.byref(dims), ctypes.byref(ext), _ptr(x), _ptr(w_lat), _ptr(w_head),
                                  _ptr(bias), _ptr(w13), _ptr(w_down), _ptr(out), _ptr(ws), ws.numel(),
                                  _stream(stream)), "moe_forward_ext")
+
+
+def moe_workspace_size_headlocal(dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_headlocal(ctypes.byref(dims), ctypes.byref(n)), "moe_workspace_size_headlocal")
+    return n.value
+
+
+def moe_prepare_weights_headlocal(dims, w_gate, w_up, w13, stream=None) -> None:
+    _dev(w_gate, w_up, w13, dtype=torch.bfloat16)
+    _check(lib().moe_prepare_weights_headlocal(ctypes.byref(dims), _ptr(w_gate), _ptr(w_up), _ptr(w13),
+                                               _stream(stream)), "moe_prepare_weights_headlocal")
+
+
+def moe_forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, logits, ws, stream=None) -> None:
+    _dev(x, w_router, w13, w_down, out, dtype=torch.bfloat16)
+    _dev(bias, logits, dtype=torch.float32)
+    _dev(topk_idx, dtype=torch.int32)
+    _check(lib().moe_forward_headlocal(ctypes.byref(dims), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w13),
+                                       _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(logits), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "moe_forward_headlocal")
 
 
 def moe_forward_host(dims, x_host, w_lat, w_head, bias, w13, w_down, out_host, ws, stream=None) -> None:

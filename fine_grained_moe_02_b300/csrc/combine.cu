@@ -23,7 +23,8 @@ __device__ __forceinline__ void acc8(float (&a)[8], const uint4& v, float g) {
 template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ gate, uint4* __restrict__ out,
-                                                      int64_t T, int d_vec, int k, int64_t rows) {
+                                                      int64_t T, int d_vec, int64_t out_ld_vec, int k,
+                                                      int64_t rows) {
   const int lane = threadIdx.x & 31;
   const int64_t wg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
       o.y = *reinterpret_cast<uint32_t*>(&b1);
       o.z = *reinterpret_cast<uint32_t*>(&b2);
       o.w = *reinterpret_cast<uint32_t*>(&b3);
-      out[t * d_vec + c] = o;
+      out[t * out_ld_vec + c] = o;
     }
   }
 }
@@ -72,10 +73,11 @@ int launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const auto* y = reinterpret_cast<const uint4*>(a.y_perm);
   auto* o = reinterpret_cast<uint4*>(a.out);
   const int64_t rows = a.T * a.k;
+  const int64_t out_ld_vec = (a.out_ld ? a.out_ld : a.d) / 8;
   if (a.k <= 6)
-    combine_kernel<6><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, a.k, rows);
+    combine_kernel<6><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, out_ld_vec, a.k, rows);
   else
-    combine_kernel<8><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, a.k, rows);
+    combine_kernel<8><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, out_ld_vec, a.k, rows);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

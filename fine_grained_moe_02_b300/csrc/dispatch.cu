@@ -191,8 +191,9 @@ __global__ void __launch_bounds__(kAssignWarps * 32) dispatch_assign_kernel(
 // One warp per token (grid-stride): read the row once into registers, write it
 // to each of its k destination rows.  16-byte vectors; d % 8 == 0.
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __restrict__ x, int64_t T, int d_vec,
-                                                              int k, const int32_t* __restrict__ row_of,
-                                                              int64_t rows, uint4* __restrict__ x_perm) {
+                                                              int64_t x_ld_vec, int k,
+                                                              const int32_t* __restrict__ row_of, int64_t rows,
+                                                              uint4* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
   for (int64_t t = warp_global; t < T; t += nwarps) {
     int dst = -1;
     if (lane < k) dst = __ldg(row_of + t * k + lane);
-    const uint4* src = x + t * d_vec;
+    const uint4* src = x + t * x_ld_vec;
     for (int c0 = 0; c0 < d_vec; c0 += 32 * kVec) {
       uint4 v[kVec];
 #pragma unroll
@@ -232,7 +233,8 @@ int launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const int d_vec = a.d / 8;
     const int64_t want = (a.T + 7) / 8;  // 8 warps (tokens) per CTA
     const int grid = static_cast<int>(want < a.sm_count * 8LL ? want : a.sm_count * 8LL);
-    dispatch_gather_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(a.x), a.T, d_vec, a.k,
+    const int64_t x_ld_vec = (a.x_ld ? a.x_ld : a.d) / 8;
+    dispatch_gather_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(a.x), a.T, d_vec, x_ld_vec, a.k,
                                                      a.row_of, a.T * a.k, reinterpret_cast<uint4*>(a.x_perm));
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

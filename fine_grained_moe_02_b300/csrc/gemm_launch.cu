@@ -65,11 +65,11 @@ int pick_bn(int n) {
 }  // namespace
 
 bool make_tmap_bf16_2d(void* tmap, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                       uint32_t box_rows) {
+                       uint32_t box_rows, uint64_t row_stride_elems) {
   auto enc = encoder();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {(row_stride_elems ? row_stride_elems : cols) * 2};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
@@ -124,6 +124,27 @@ int launch_route_folded(const RouteArgs& a, const uint16_t* w_router, cudaStream
   GemmShape sh{2 * a.d, 2 * a.d, bn, 1, nullptr, static_cast<int>(a.T), a.status, nullptr, a.d};
   EpiTopK::Params ep = make_topk_params(a);
   const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
+  return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream);
+}
+
+int launch_router_head(const uint16_t* x_head, int64_t x_ld, const uint16_t* w_router_head, const float* bias_head,
+                       int64_t T, int head_dim, int E, int k, int32_t* idx, float* gate, float* logits, int* status,
+                       int sm_count, cudaStream_t stream) {
+  const int64_t m_tiles = (T + kBM - 1) / kBM;
+  const int bn = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_2d(&ta, x_head, head_dim, T, kBK, kBM, x_ld)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, w_router_head, head_dim, E, kBK, bn)) return MOE_ERR_CUDA;
+  GemmShape sh{head_dim, head_dim, bn, 1, nullptr, static_cast<int>(T), status};
+  TopKParams ep{};
+  ep.bias = bias_head;
+  ep.logits = logits;
+  ep.idx = idx;
+  ep.gate = gate;
+  ep.E = E;
+  ep.k = k;
+  ep.status = status;
+  const int grid = static_cast<int>(m_tiles < sm_count ? m_tiles : sm_count);
   return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream);
 }
 

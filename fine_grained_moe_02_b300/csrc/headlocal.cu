@@ -1,0 +1,167 @@
+// Head-local MultiHead MoE: the hidden vector (d = n_heads * head_dim) is split
+// into head slices; head j routes its own slice over its own E experts (router
+// GEMM + fused top-k), sorts its tokens, runs its head-local SwiGLU experts
+// (head_dim -> inter -> head_dim, grouped tcgen05 GEMMs) and combines into its
+// head_dim columns of out.  The heads run one after another on the caller's
+// stream and reuse one set of per-head buffers in the workspace.
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "internal.h"
+#include "moe.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_hl(const moe_dims* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 1 || d->n_heads < 1 || d->head_dim < 1 || d->E < 1 || d->inter < 1 || d->top_k < 1)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(d->n_heads) * d->head_dim != d->d) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->head_dim % 64 != 0 || d->inter % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->E > kMaxExperts || d->top_k > kMaxTopK || d->top_k > d->E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d->T * d->top_k >= (static_cast<int64_t>(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(d->E) * 2 * d->inter >= (static_cast<int64_t>(1) << 31) ||
+      static_cast<int64_t>(d->n_heads) * d->E * d->head_dim >= (static_cast<int64_t>(1) << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+struct HlLayout {
+  size_t disp, idx, gate, offsets, row_of, src, xperm, act, end;
+};
+
+HlLayout hl_layout(const moe_dims* d) {
+  HlLayout l;
+  const size_t Tk = static_cast<size_t>(d->T) * d->top_k;
+  l.disp = kAlign;
+  l.idx = align_up(l.disp + dispatch_scratch_bytes(d->T, d->E), kAlign);
+  l.gate = align_up(l.idx + Tk * 4, kAlign);
+  l.offsets = align_up(l.gate + Tk * 4, kAlign);
+  l.row_of = align_up(l.offsets + (static_cast<size_t>(d->E) + 1) * 4, kAlign);
+  l.src = align_up(l.row_of + Tk * 4, kAlign);
+  l.xperm = align_up(l.src + Tk * 4, kAlign);
+  l.act = align_up(l.xperm + Tk * d->head_dim * 2, kAlign);
+  l.end = align_up(l.act + Tk * d->inter * 2, kAlign);
+  return l;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_workspace_size_headlocal(const moe_dims* dims, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  const int rc = check_hl(dims);
+  if (rc != MOE_OK) return rc;
+  *bytes = hl_layout(dims).end;
+  return MOE_OK;
+}
+
+int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
+                                  void* stream) {
+  int rc = check_hl(dims);
+  if (rc != MOE_OK) return rc;
+  if (w_gate == nullptr || w_up == nullptr || w13 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w13)) return MOE_ERR_MISALIGNED;
+  // the n_heads * E head-local experts interleave exactly like E experts of width head_dim
+  return launch_prepare_w13(w_gate, w_up, w13, dims->n_heads * dims->E, dims->inter, dims->head_dim,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                          const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx,
+                          float* logits, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_hl(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_router == nullptr || w13 == nullptr || w_down == nullptr || out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w13) || !aligned16(w_down) || !aligned16(out) ||
+      !aligned16(ws) || (bias != nullptr && !aligned16(bias)) || (topk_idx != nullptr && !aligned16(topk_idx)) ||
+      (logits != nullptr && !aligned16(logits)))
+    return MOE_ERR_MISALIGNED;
+  const HlLayout l = hl_layout(dims);
+  if (ws_bytes < l.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return MOE_ERR_CUDA;
+
+  const int H = dims->n_heads, Dh = dims->head_dim, E = dims->E, I = dims->inter, k = dims->top_k;
+  const int64_t T = dims->T, Tk = T * k;
+  int* status = static_cast<int*>(ws);
+  const int64_t nblk_e = static_cast<int64_t>(dispatch_scratch_bytes(T, E) / 8);
+  for (int j = 0; j < H; ++j) {
+    const moe_bf16* xj = x + static_cast<int64_t>(j) * Dh;
+    int32_t* idx = topk_idx != nullptr ? topk_idx + static_cast<int64_t>(j) * Tk : at<int32_t>(ws, l.idx);
+    float* gate = at<float>(ws, l.gate);
+    float* lg = logits != nullptr ? logits + static_cast<int64_t>(j) * T * E : nullptr;
+    rc = launch_router_head(xj, dims->d, w_router + static_cast<int64_t>(j) * E * Dh,
+                            bias != nullptr ? bias + static_cast<int64_t>(j) * E : nullptr, T, Dh, E, k, idx, gate, lg,
+                            status, sms, s);
+    if (rc != MOE_OK) return rc;
+
+    DispatchArgs da{};
+    da.x = xj;
+    da.x_ld = dims->d;
+    da.topk_idx = idx;
+    da.T = T;
+    da.d = Dh;
+    da.k = k;
+    da.E = E;
+    da.offsets = at<int32_t>(ws, l.offsets);
+    da.row_of = at<int32_t>(ws, l.row_of);
+    da.src_token = at<int32_t>(ws, l.src);
+    da.x_perm = at<uint16_t>(ws, l.xperm);
+    da.block_counts = at<int32_t>(ws, l.disp);
+    da.block_base = at<int32_t>(ws, l.disp) + nblk_e;
+    da.status = status;
+    da.sm_count = sms;
+    if ((rc = launch_dispatch(da, s)) != MOE_OK) return rc;
+
+    FfnArgs fa{};
+    fa.offsets = da.offsets;
+    fa.rows = Tk;
+    fa.d = Dh;
+    fa.I = I;
+    fa.E = E;
+    fa.status = status;
+    fa.sm_count = sms;
+    fa.x_perm = da.x_perm;
+    fa.w13 = w13 + static_cast<int64_t>(j) * E * 2 * I * Dh;
+    fa.act = at<uint16_t>(ws, l.act);
+    if ((rc = launch_gemm1(fa, s)) != MOE_OK) return rc;
+    fa.w_down = w_down + static_cast<int64_t>(j) * E * Dh * I;
+    fa.y_perm = da.x_perm;  // x_perm is dead after GEMM-1
+    if ((rc = launch_gemm2(fa, s)) != MOE_OK) return rc;
+
+    CombineArgs ca{};
+    ca.y_perm = fa.y_perm;
+    ca.row_of = da.row_of;
+    ca.gate = gate;
+    ca.out = out + static_cast<int64_t>(j) * Dh;
+    ca.out_ld = dims->d;
+    ca.T = T;
+    ca.d = Dh;
+    ca.k = k;
+    ca.sm_count = sms;
+    if ((rc = launch_combine(ca, s)) != MOE_OK) return rc;
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

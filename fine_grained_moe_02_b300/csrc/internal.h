@@ -19,6 +19,7 @@ struct DispatchArgs {
   int32_t* row_of;
   int32_t* src_token;
   uint16_t* x_perm;        // nullptr: permutation only
+  int64_t x_ld;            // row stride of x in elements (0: d)
   int32_t* block_counts;   // scratch [nblk * E]
   int32_t* block_base;     // scratch [nblk * E]
   int* status;
@@ -74,6 +75,7 @@ struct CombineArgs {
   uint16_t* out;
   int64_t T;
   int d, k;
+  int64_t out_ld;          // row stride of out in elements (0: d)
   int sm_count;
 };
 
@@ -96,6 +98,12 @@ int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w
 
 // cuTensorMapEncodeTiled, resolved once through the runtime (no -lcuda).
 bool make_tmap_bf16_2d(void* tmap /* CUtensorMap* */, const void* base, uint64_t cols, uint64_t rows,
-                       uint32_t box_cols, uint32_t box_rows);
+                       uint32_t box_cols, uint32_t box_rows, uint64_t row_stride_elems = 0);
+
+// Head-local router for one head: s = x_j W_router[j]^T + b[j] over the strided
+// head view of x, with the fused top-k epilogue (idx/gate [T, k]).
+int launch_router_head(const uint16_t* x_head, int64_t x_ld, const uint16_t* w_router_head, const float* bias_head,
+                       int64_t T, int head_dim, int E, int k, int32_t* idx, float* gate, float* logits, int* status,
+                       int sm_count, cudaStream_t stream);
 
 }  // namespace moe

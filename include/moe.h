@@ -315,6 +315,29 @@ int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x,
                     const moe_bf16* w_head, const float* bias, const moe_bf16* w13, const moe_bf16* w_down,
                     moe_bf16* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Head-local MultiHead MoE (36kr article, section 02: the hidden
+ * representation split into heads, each head choosing its own experts in its
+ * own low-dimensional subspace, the head results fused back).  Here
+ * dims->d = n_heads * head_dim and dims->E is the number of experts PER
+ * HEAD; head j's slice x_j = x[:, j*head_dim : (j+1)*head_dim] is scored by
+ * its own router, s_j = x_j W_router[j]^T + bias[j], softmax, top_k (ties
+ * to the lowest index), renormalised gates; its chosen head-local SwiGLU
+ * experts (head_dim -> inter -> head_dim) are combined into out's columns
+ * of head j (concatenation of the heads).
+ *   w_router [n_heads, E, head_dim] bf16, bias [n_heads, E] fp32 or NULL
+ *   w13 [n_heads, E, 2*inter, head_dim] from moe_prepare_weights_headlocal
+ *   w_down [n_heads, E, head_dim, inter] bf16, out [T, d] bf16
+ *   topk_idx [n_heads, T, top_k] int32 or NULL (written: each head's choice)
+ *   logits [n_heads, T, E] fp32 or NULL (written: each head's scores)
+ * Rules: head_dim % 64 == 0, inter % 64 == 0, E <= 256, top_k <= min(8, E).
+ * The heads run in sequence on `stream`, reusing one set of buffers. */
+int moe_workspace_size_headlocal(const moe_dims* dims, size_t* bytes);
+int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
+                                  void* stream);
+int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                          const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx,
+                          float* logits, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_forward for a caller whose activations live in host memory: copies
  * x_host [T, d] to the device, runs the layer, copies out to out_host [T, d]
  * and synchronises `stream`.  Weights are device pointers.  Host buffers
