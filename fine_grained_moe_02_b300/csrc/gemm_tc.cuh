@@ -15,6 +15,13 @@
 // (tile = blockIdx.x + i * gridDim.x) in group-major, m-major, n-minor order
 // so that CTAs running at the same time share A and B tiles through L2.
 //
+// CL = 2 (cluster of two CTAs on adjacent m-blocks of the same group and
+// n-tile): each CTA loads its own A rows and one half of the shared B tile,
+// multicasting that half into both CTAs' shared memory, so the pair reads B
+// from L2 once (a third less L2-to-SM traffic per tile).  Each CTA's MMA
+// commit frees the stage in both CTAs.  A group with an odd number of
+// m-blocks pairs its last one with an empty partner (computed, never stored).
+//
 // Every wait is bounded (see ptx::mbar_wait): on a timeout the kernel sets
 // MOE_DEV_TIMEOUT in the status word, the other roles stop, in-flight TMA
 // loads and MMAs are drained (again with a limit), TMEM is freed and the
@@ -92,7 +99,7 @@ struct TileCoord {
 
 template <int BN>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, const int* s_tile, int groups,
-                                                 int n_tiles) {
+                                                 int n_tiles, int cl = 1, int crank = 0) {
   // largest g with s_tile[g] <= tile
   int lo = 0, hi = groups - 1;
   while (lo < hi) {
@@ -104,7 +111,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, con
   const int local = tile - s_tile[lo];
   c.m_blk = local / n_tiles;
   c.n_blk = local - c.m_blk * n_tiles;
-  c.row0 = s_row[lo] + c.m_blk * kBM;
+  c.row0 = s_row[lo] + (c.m_blk * cl + crank) * kBM;
   c.row_end = s_row[lo + 1];
   return c;
 }
@@ -114,7 +121,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, con
 //   template <int BN> static __device__ void run(const Params&, const TileCoord&, uint32_t taddr,
 //                                                 int row_in_tile, EpiCtx&);
 // taddr addresses this thread's lane (= tile row) at the accumulator's column 0.
-template <int BN, class Epi>
+template <int BN, class Epi, int CL = 1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d, GemmShape shape, typename Epi::Params ep) {
@@ -134,10 +141,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ int s_tile[kMaxGroups + 1];
   __shared__ int s_total;
 
+  static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = shape.N / BN;
   const int groups = shape.groups;
+  const int crank = CL == 2 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int first_tile = CL == 2 ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int tile_step = CL == 2 ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  constexpr uint16_t kPair = 0x3;
 
   // ---- group table: row offsets and tile prefix (all threads, then warp 0 scans)
   for (int i = threadIdx.x; i <= groups; i += blockDim.x)
@@ -154,7 +166,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       if (g < groups) {
         const int a = s_row[g], b = s_row[g + 1];
         if (a < 0 || b < a || b > shape.M) bad = true;
-        else cnt = ((b - a + kBM - 1) / kBM) * n_tiles;
+        else cnt = ((b - a + CL * kBM - 1) / (CL * kBM)) * n_tiles;
       }
       int incl = cnt;
 #pragma unroll
@@ -175,7 +187,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), CL);  // every CTA's MMA frees the stage in all CTAs
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
@@ -195,6 +207,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before any multicast reaches them
+  if constexpr (CL == 2) ptx::cluster_sync();
   ptx::tc_fence_after();
 
   const uint32_t tmem_base = s_tmem;
@@ -211,7 +225,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     uint32_t phase = 0;
     uint32_t filled = 0, last_par = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = first_tile; tile < total && ok; tile += tile_step) {
       const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
       const int b_row = c.group * shape.N + c.n_blk * BN;
       int src[4];
@@ -269,8 +283,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       uint32_t filled = 0;       // bit s: stage s was filled at least once
       uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok && !shape.selftest_stall; tile += gridDim.x) {
-        const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
+      for (int tile = first_tile; tile < total && ok && !shape.selftest_stall; tile += tile_step) {
+        const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles, CL, crank);
         const int b_row = c.group * shape.N + c.n_blk * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, wait_ns)) {
@@ -283,7 +297,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
           const uint32_t sb = sa + S::kABytes;
           const int k = kb * kBK;
           ptx::tma_load_2d(sa, &tmap_a, shape.K_A > 0 ? k % shape.K_A : k, c.row0, fb, pol_a);
-          ptx::tma_load_2d(sb, &tmap_b, k % shape.K_B, b_row, fb, pol_b);
+          if constexpr (CL == 2) {  // this CTA's half of B, into both CTAs
+            constexpr int kHalf = BN / 2;
+            ptx::tma_load_2d_multicast(sb + crank * kHalf * 128, &tmap_b, k % shape.K_B, b_row + crank * kHalf, fb,
+                                       kPair, pol_b);
+          } else {
+            ptx::tma_load_2d(sb, &tmap_b, k % shape.K_B, b_row, fb, pol_b);
+          }
           filled |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -311,7 +331,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = first_tile; tile < total && ok; tile += tile_step) {
         if (!ptx::mbar_wait(ptx::smem_u32(&tempty_bar[acc]), acc_phase ^ 1, &s_abort, wait_ns)) {
           ok = false;
           break;
@@ -332,7 +352,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             const uint64_t db = ptx::sw128_desc(sb + kk * kUK * 2);
             ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+          if constexpr (CL == 2) ptx::mma_commit_multicast(ptx::smem_u32(&empty_bar[stage]), kPair);
+          else ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -357,7 +378,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     EpiCtx ctx{&tmap_d, ptx::smem_u32(smem + STAGES * S::kStageBytes + quad * kOutChunkBytes), lane, quad, false};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = first_tile; tile < total; tile += tile_step) {
       const bool ok = ptx::mbar_wait(ptx::smem_u32(&tfull_bar[acc]), acc_phase, &s_abort, wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) atomicOr(shape.status, MOE_DEV_TIMEOUT);
@@ -365,7 +386,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         break;
       }
       ptx::tc_fence_after();
-      const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
+      const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles, CL, crank);
       Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile, ctx);
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[acc]));
@@ -383,6 +404,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, S::kTmemCols);
   }
+  // neither CTA may exit while its peer can still multicast into it or
+  // arrive on its barriers
+  if constexpr (CL == 2) ptx::cluster_sync();
 }
 
 }  // namespace moe
