@@ -24,11 +24,20 @@ template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
                                                       const float* __restrict__ gate, uint4* __restrict__ out,
                                                       int64_t T, int d_vec, int64_t out_ld_vec, int k,
-                                                      int64_t rows) {
+                                                      int64_t rows, int heads) {
   const int lane = threadIdx.x & 31;
   const int64_t wg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t t = wg; t < T; t += nw) {
+  const uint4* y0 = y;
+  const int32_t* row_of0 = row_of;
+  const float* gate0 = gate;
+  uint4* out0 = out;
+  for (int64_t ht = wg; ht < T * heads; ht += nw) {
+    const int64_t h = ht / T, t = ht - h * T;  // (head, token): head h's outputs go to its d columns
+    y = y0 + h * rows * d_vec;
+    row_of = row_of0 + h * T * k;
+    gate = gate0 + h * T * k;
+    out = out0 + h * d_vec;
     int r_l = -1;
     float g_l = 0.f;
     if (lane < k) {
@@ -68,16 +77,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
 
 int launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const int d_vec = a.d / 8;
-  const int64_t want = (a.T + 7) / 8;
+  const int64_t want = (a.T * (a.heads > 1 ? a.heads : 1) + 7) / 8;
   const int grid = static_cast<int>(want < a.sm_count * 8LL ? want : a.sm_count * 8LL);
   const auto* y = reinterpret_cast<const uint4*>(a.y_perm);
   auto* o = reinterpret_cast<uint4*>(a.out);
   const int64_t rows = a.T * a.k;
   const int64_t out_ld_vec = (a.out_ld ? a.out_ld : a.d) / 8;
+  const int heads = a.heads > 1 ? a.heads : 1;
   if (a.k <= 6)
-    combine_kernel<6><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, out_ld_vec, a.k, rows);
+    combine_kernel<6><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, out_ld_vec, a.k, rows, heads);
   else
-    combine_kernel<8><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, out_ld_vec, a.k, rows);
+    combine_kernel<8><<<grid, 256, 0, stream>>>(y, a.row_of, a.gate, o, a.T, d_vec, out_ld_vec, a.k, rows, heads);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -40,6 +40,9 @@ __device__ __forceinline__ void load_slots(const int32_t* __restrict__ row, int 
 __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k,
                                                             int E, int32_t* __restrict__ block_counts,
                                                             int* status) {
+  // head blockIdx.y of a batch of independent sorts
+  topk_idx += static_cast<int64_t>(blockIdx.y) * T * k;
+  block_counts += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
   __shared__ int hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -63,6 +66,10 @@ __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __res
 __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __restrict__ block_counts, int nblk,
                                                              int E, int32_t* __restrict__ block_base,
                                                              int32_t* __restrict__ offsets) {
+  // head blockIdx.x of a batch of independent sorts
+  block_counts += static_cast<int64_t>(blockIdx.x) * nblk * E;
+  block_base += static_cast<int64_t>(blockIdx.x) * nblk * E;
+  offsets += static_cast<int64_t>(blockIdx.x) * (E + 1);
   __shared__ int total[kMaxExperts];
   __shared__ int off[kMaxExperts + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -110,6 +117,11 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __re
 __global__ void __launch_bounds__(kAssignWarps * 32) dispatch_assign_kernel(
     const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, const int32_t* __restrict__ block_base,
     int32_t* __restrict__ row_of, int32_t* __restrict__ src_token) {
+  // head blockIdx.y of a batch of independent sorts
+  topk_idx += static_cast<int64_t>(blockIdx.y) * T * k;
+  block_base += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
+  row_of += static_cast<int64_t>(blockIdx.y) * T * k;
+  src_token += static_cast<int64_t>(blockIdx.y) * T * k;
   __shared__ int wcnt[kAssignWarps][kMaxExperts];   // per-warp counts, then per-warp cursors
   __shared__ unsigned mask[kAssignWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,17 +203,19 @@ __global__ void __launch_bounds__(kAssignWarps * 32) dispatch_assign_kernel(
 // One warp per token (grid-stride): read the row once into registers, write it
 // to each of its k destination rows.  16-byte vectors; d % 8 == 0.
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __restrict__ x, int64_t T, int d_vec,
-                                                              int64_t x_ld_vec, int k,
+                                                              int64_t x_ld_vec, int64_t x_head_vec, int heads, int k,
                                                               const int32_t* __restrict__ row_of, int64_t rows,
                                                               uint4* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   constexpr int kVec = 8;  // uint4 per lane per pass (4 KB per warp)
-  for (int64_t t = warp_global; t < T; t += nwarps) {
+  for (int64_t ht = warp_global; ht < T * heads; ht += nwarps) {
+    const int64_t h = ht / T, t = ht - h * T;  // (head, token)
     int dst = -1;
-    if (lane < k) dst = __ldg(row_of + t * k + lane);
-    const uint4* src = x + t * x_ld_vec;
+    if (lane < k) dst = __ldg(row_of + (h * T + t) * k + lane);
+    const uint4* src = x + h * x_head_vec + t * x_ld_vec;
+    uint4* x_perm_h = x_perm + h * rows * d_vec;
     for (int c0 = 0; c0 < d_vec; c0 += 32 * kVec) {
       uint4 v[kVec];
 #pragma unroll
@@ -212,7 +226,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
       for (int s = 0; s < k; ++s) {
         const int r = __shfl_sync(0xffffffffu, dst, s);
         if (r < 0 || r >= rows) continue;
-        uint4* o = x_perm + static_cast<int64_t>(r) * d_vec;
+        uint4* o = x_perm_h + static_cast<int64_t>(r) * d_vec;
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
           const int c = c0 + j * 32 + lane;
@@ -225,17 +239,19 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
 
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   const int nblk = static_cast<int>((a.T + kTokBlock - 1) / kTokBlock);
-  dispatch_hist_kernel<<<nblk, 256, 0, stream>>>(a.topk_idx, a.T, a.k, a.E, a.block_counts, a.status);
-  dispatch_scan_kernel<<<1, 1024, 0, stream>>>(a.block_counts, nblk, a.E, a.block_base, a.offsets);
-  dispatch_assign_kernel<<<nblk, kAssignWarps * 32, 0, stream>>>(a.topk_idx, a.T, a.k, a.E, a.block_base,
-                                                                  a.row_of, a.src_token);
+  const int heads = a.heads > 1 ? a.heads : 1;
+  dispatch_hist_kernel<<<dim3(nblk, heads), 256, 0, stream>>>(a.topk_idx, a.T, a.k, a.E, a.block_counts, a.status);
+  dispatch_scan_kernel<<<heads, 1024, 0, stream>>>(a.block_counts, nblk, a.E, a.block_base, a.offsets);
+  dispatch_assign_kernel<<<dim3(nblk, heads), kAssignWarps * 32, 0, stream>>>(a.topk_idx, a.T, a.k, a.E,
+                                                                               a.block_base, a.row_of, a.src_token);
   if (a.x_perm != nullptr) {
     const int d_vec = a.d / 8;
-    const int64_t want = (a.T + 7) / 8;  // 8 warps (tokens) per CTA
+    const int64_t want = (a.T * heads + 7) / 8;  // 8 warps (tokens) per CTA
     const int grid = static_cast<int>(want < a.sm_count * 8LL ? want : a.sm_count * 8LL);
     const int64_t x_ld_vec = (a.x_ld ? a.x_ld : a.d) / 8;
-    dispatch_gather_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(a.x), a.T, d_vec, x_ld_vec, a.k,
-                                                     a.row_of, a.T * a.k, reinterpret_cast<uint4*>(a.x_perm));
+    dispatch_gather_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(a.x), a.T, d_vec, x_ld_vec,
+                                                     a.x_head_off / 8, heads, a.k, a.row_of, a.T * a.k,
+                                                     reinterpret_cast<uint4*>(a.x_perm));
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -244,5 +260,7 @@ size_t dispatch_scratch_bytes(int64_t T, int E) {
   const int64_t nblk = (T + kTokBlock - 1) / kTokBlock;
   return static_cast<size_t>(2 * nblk * E) * sizeof(int32_t);
 }
+
+size_t dispatch_counter_cells(int64_t T, int E) { return static_cast<size_t>((T + kTokBlock - 1) / kTokBlock) * E; }
 
 }  // namespace moe

@@ -196,6 +196,9 @@ struct TopKParams {
   int n_mod;
   int ebeg[kMaxModalities], eend[kMaxModalities];
   int* status;                   // MOE_DEV_BAD_MODALITY for an id outside [0, n_mod)
+  // Batched problems (one per GEMM group, rows g*T .. g*T+T-1 of the tile
+  // space): outputs of group g start at idx + g*T*k_out, logits + g*T*E, bias + g*E.
+  int T;                         // rows per group (0: not batched)
 };
 
 inline TopKParams make_topk_params(const RouteArgs& a) {
@@ -313,6 +316,17 @@ struct EpiTopK {
   static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
                                              EpiCtx&) {
     const int row = c.row0 + r;
+    if (p.T > 0) {  // batched: group c.group owns its own outputs
+      TopKParams q = p;
+      const int64_t g = c.group;
+      const int ko = p.k_out > 0 ? p.k_out : p.k;
+      q.idx = p.idx + g * p.T * ko;
+      q.gate = p.gate + g * p.T * ko;
+      if (p.logits != nullptr) q.logits = p.logits + g * p.T * p.E;
+      if (p.bias != nullptr) q.bias = p.bias + g * p.E;
+      topk_row<BN>(q, taddr, row - static_cast<int>(g) * p.T, row < c.row_end);
+      return;
+    }
     topk_row<BN>(p, taddr, row, row < c.row_end);
   }
 };

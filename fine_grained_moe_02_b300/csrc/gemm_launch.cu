@@ -33,8 +33,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 template <int BN, class Epi, int CL = 1>
 int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmShape& shape,
-             const typename Epi::Params& ep, int grid, cudaStream_t stream) {
+             const typename Epi::Params& ep, int grid, cudaStream_t stream, int b_box_rows) {
   using S = GemmSmem<BN>;
+  // the B tensor map must deliver exactly this kernel's per-CTA B slice, or
+  // the stage byte count and the shared-memory ring would disagree
+  if (b_box_rows != BN / CL) return MOE_ERR_UNSUPPORTED_SHAPE;
   auto kern = gemm_tc_kernel<BN, Epi, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynBytes) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -74,13 +77,14 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
 
 template <class Epi>
 int run_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
-                const GemmShape& shape, const typename Epi::Params& ep, int grid, cudaStream_t stream) {
+                const GemmShape& shape, const typename Epi::Params& ep, int grid, cudaStream_t stream,
+                int b_box_rows) {
   switch (bn) {
-    case 256: return run_gemm<256, Epi>(ta, tb, td, shape, ep, grid, stream);
-    case 128: return run_gemm<128, Epi>(ta, tb, td, shape, ep, grid, stream);
-    case 64: return run_gemm<64, Epi>(ta, tb, td, shape, ep, grid, stream);
-    case 32: return run_gemm<32, Epi>(ta, tb, td, shape, ep, grid, stream);
-    case 16: return run_gemm<16, Epi>(ta, tb, td, shape, ep, grid, stream);
+    case 256: return run_gemm<256, Epi>(ta, tb, td, shape, ep, grid, stream, b_box_rows);
+    case 128: return run_gemm<128, Epi>(ta, tb, td, shape, ep, grid, stream, b_box_rows);
+    case 64: return run_gemm<64, Epi>(ta, tb, td, shape, ep, grid, stream, b_box_rows);
+    case 32: return run_gemm<32, Epi>(ta, tb, td, shape, ep, grid, stream, b_box_rows);
+    case 16: return run_gemm<16, Epi>(ta, tb, td, shape, ep, grid, stream, b_box_rows);
     default: return MOE_ERR_UNSUPPORTED_SHAPE;
   }
 }
@@ -137,8 +141,8 @@ int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream) {
     EpiHiLo::Params ep{a.hl, 2LL * a.L, a.L};
     const int64_t tiles = m_tiles * (a.L / bn);
     const int grid = static_cast<int>(tiles < a.sm_count ? tiles : a.sm_count);
-    const int rc = pair ? run_gemm<256, EpiHiLo, 2>(ta, tb, td, sh, ep, grid, stream)
-                        : run_gemm_bn<EpiHiLo>(bn, ta, tb, td, sh, ep, grid, stream);
+    const int rc = pair ? run_gemm<256, EpiHiLo, 2>(ta, tb, td, sh, ep, grid, stream, bn / 2)
+                        : run_gemm_bn<EpiHiLo>(bn, ta, tb, td, sh, ep, grid, stream, bn);
     if (rc != MOE_OK) return rc;
   }
   {
@@ -148,7 +152,7 @@ int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream) {
     GemmShape sh{2 * a.L, a.L, bn, 1, nullptr, static_cast<int>(a.T), a.status};
     EpiTopK::Params ep = make_topk_params(a);
     const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
-    return run_gemm_bn<EpiTopK>(bn, ta, tb, ta /* no bulk output */, sh, ep, grid, stream);
+    return run_gemm_bn<EpiTopK>(bn, ta, tb, ta /* no bulk output */, sh, ep, grid, stream, bn);
   }
 }
 
@@ -163,28 +167,33 @@ int launch_route_folded(const RouteArgs& a, const uint16_t* w_router, cudaStream
   GemmShape sh{2 * a.d, 2 * a.d, bn, 1, nullptr, static_cast<int>(a.T), a.status, nullptr, a.d};
   EpiTopK::Params ep = make_topk_params(a);
   const int grid = static_cast<int>(m_tiles < a.sm_count ? m_tiles : a.sm_count);
-  return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream);
+  return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream, bn);
 }
 
-int launch_router_head(const uint16_t* x_head, int64_t x_ld, const uint16_t* w_router_head, const float* bias_head,
-                       int64_t T, int head_dim, int E, int k, int32_t* idx, float* gate, float* logits, int* status,
-                       int sm_count, cudaStream_t stream) {
+// All heads' routers of the head-local layer in one launch: problem h is
+// s_h = x[:, h*Dh : (h+1)*Dh] W_router[h]^T (+ bias[h]) with the top-k epilogue,
+// outputs idx/gate [H, T, k], logits [H, T, E].
+int launch_router_headlocal(const uint16_t* x, int64_t T, int d, int H, int Dh, const uint16_t* w_router, int E,
+                            int k, const float* bias, int32_t* idx, float* gate, float* logits, int* status,
+                            int sm_count, cudaStream_t stream) {
   const int64_t m_tiles = (T + kBM - 1) / kBM;
   const int bn = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16_2d(&ta, x_head, head_dim, T, kBK, kBM, x_ld)) return MOE_ERR_CUDA;
-  if (!make_tmap_bf16_2d(&tb, w_router_head, head_dim, E, kBK, bn)) return MOE_ERR_CUDA;
-  GemmShape sh{head_dim, head_dim, bn, 1, nullptr, static_cast<int>(T), status};
+  if (!make_tmap_bf16_2d(&ta, x, d, T, kBK, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, w_router, Dh, static_cast<uint64_t>(H) * E, kBK, bn)) return MOE_ERR_CUDA;
+  GemmShape sh{Dh, Dh, bn, H, nullptr, static_cast<int>(T), status, nullptr, 0, 0, 0, 1, Dh, E};
   TopKParams ep{};
-  ep.bias = bias_head;
+  ep.bias = bias;
   ep.logits = logits;
   ep.idx = idx;
   ep.gate = gate;
   ep.E = E;
   ep.k = k;
   ep.status = status;
-  const int grid = static_cast<int>(m_tiles < sm_count ? m_tiles : sm_count);
-  return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream);
+  ep.T = static_cast<int>(T);
+  const int64_t tiles = m_tiles * H;
+  const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+  return run_gemm_bn<EpiTopK>(bn, ta, tb, ta, sh, ep, grid, stream, bn);
 }
 
 // Expert GEMM-1 over ragged groups (device offsets), SwiGLU fused: act = silu(x Wg^T) * (x Wu^T).
@@ -200,8 +209,9 @@ int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
   if (!make_tmap_bf16_2d(&td, a.act, a.I, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status};
   EpiSwiGLU::Params ep{a.act, a.I};
-  return pair ? run_gemm<256, EpiSwiGLU, 2>(ta, tb, td, sh, ep, a.sm_count, stream)
-              : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream);
+  if (pair) return run_gemm<256, EpiSwiGLU, 2>(ta, tb, td, sh, ep, a.sm_count, stream, bn / 2);
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn)
+                     : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
 // Expert GEMM-1 with the row gather fused into the A loads: A row r is
@@ -217,8 +227,8 @@ int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream) {
   if (!make_tmap_bf16_2d(&td, a.act, a.I, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status, a.src_token};
   EpiSwiGLU::Params ep{a.act, a.I};
-  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream)
-                     : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream);
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn)
+                     : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
 // Expert GEMM-2 over ragged groups: y_perm = act Wd^T.
@@ -233,8 +243,8 @@ int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
   if (!make_tmap_bf16_2d(&td, a.y_perm, a.d, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
   EpiStoreBf16::Params ep{a.y_perm, a.d};
-  return pair ? run_gemm<256, EpiStoreBf16, 2>(ta, tb, td, sh, ep, a.sm_count, stream)
-              : run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream);
+  return pair ? run_gemm<256, EpiStoreBf16, 2>(ta, tb, td, sh, ep, a.sm_count, stream, bn / 2)
+              : run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
 // Self-test of the bounded waits: one 128 x 256 x 64 tile whose producer
@@ -250,7 +260,7 @@ int launch_selftest_timeout(uint16_t* scratch, int* status, uint64_t limit_ns, c
   if (!make_tmap_bf16_2d(&td, d, 256, 128, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{64, 64, 256, 1, nullptr, 128, status, nullptr, 0, limit_ns, 1};
   EpiStoreBf16::Params ep{d, 256};
-  return run_gemm<256, EpiStoreBf16>(ta, tb, td, sh, ep, 1, stream);
+  return run_gemm<256, EpiStoreBf16>(ta, tb, td, sh, ep, 1, stream, 256);
 }
 
 // w13[e, 128b + j] = j < 64 ? w_gate[e, 64b + j] : w_up[e, 64b + j - 64]   (rows of d)

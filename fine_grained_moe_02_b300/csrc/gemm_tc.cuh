@@ -64,6 +64,12 @@ struct GemmShape {
   // Self-test only: the producer issues no loads, so the other roles' waits
   // run out and the timeout path (status bit, drain, TMEM release) executes.
   int selftest_stall;
+  // Batched dense mode (offsets == nullptr, batched != 0): `groups`
+  // independent problems over the same M rows of A; problem g reads A's
+  // columns from g * a_col_stride and B's rows from g * b_group_rows.
+  int batched;
+  int a_col_stride;
+  int b_group_rows;
 };
 
 template <int BN>
@@ -152,8 +158,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   constexpr uint16_t kPair = 0x3;
 
   // ---- group table: row offsets and tile prefix (all threads, then warp 0 scans)
+  // (batched dense mode: every group spans rows [0, M); decode_tile maps them)
   for (int i = threadIdx.x; i <= groups; i += blockDim.x)
-    s_row[i] = shape.offsets ? __ldg(shape.offsets + i) : (i == 0 ? 0 : shape.M);
+    s_row[i] = shape.offsets ? __ldg(shape.offsets + i) : (shape.batched ? i * shape.M : (i == 0 ? 0 : shape.M));
   if (threadIdx.x == 0) s_abort = 0;
   __syncthreads();
   if (warp == 0) {
@@ -165,7 +172,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       int cnt = 0;
       if (g < groups) {
         const int a = s_row[g], b = s_row[g + 1];
-        if (a < 0 || b < a || b > shape.M) bad = true;
+        if (a < 0 || b < a || b > (shape.batched ? groups * shape.M : shape.M)) bad = true;
         else cnt = ((b - a + CL * kBM - 1) / (CL * kBM)) * n_tiles;
       }
       int incl = cnt;
@@ -285,7 +292,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       bool ok = true;
       for (int tile = first_tile; tile < total && ok && !shape.selftest_stall; tile += tile_step) {
         const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles, CL, crank);
-        const int b_row = c.group * shape.N + c.n_blk * BN;
+        const int b_row = c.group * (shape.b_group_rows ? shape.b_group_rows : shape.N) + c.n_blk * BN;
+        const int a_row = shape.batched ? c.row0 - c.group * shape.M : c.row0;
+        const int a_col = shape.batched ? c.group * shape.a_col_stride : 0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, wait_ns)) {
             ok = false;
@@ -296,7 +305,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
           const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
           const uint32_t sb = sa + S::kABytes;
           const int k = kb * kBK;
-          ptx::tma_load_2d(sa, &tmap_a, shape.K_A > 0 ? k % shape.K_A : k, c.row0, fb, pol_a);
+          ptx::tma_load_2d(sa, &tmap_a, a_col + (shape.K_A > 0 ? k % shape.K_A : k), a_row, fb, pol_a);
           if constexpr (CL == 2) {  // this CTA's half of B, into both CTAs
             constexpr int kHalf = BN / 2;
             ptx::tma_load_2d_multicast(sb + crank * kHalf * 128, &tmap_b, k % shape.K_B, b_row + crank * kHalf, fb,

@@ -38,17 +38,21 @@ struct HlLayout {
   size_t disp, idx, gate, offsets, row_of, src, xperm, act, end;
 };
 
+// Per-head arrays side by side: idx/gate/row_of/src [H, T, k], offsets [H, E+1],
+// x_perm (then y_perm) [H, T*k, head_dim], dispatch counters [2][H][nblk][E];
+// act [T*k, inter] is reused head by head.
 HlLayout hl_layout(const moe_dims* d) {
   HlLayout l;
+  const size_t H = d->n_heads;
   const size_t Tk = static_cast<size_t>(d->T) * d->top_k;
   l.disp = kAlign;
-  l.idx = align_up(l.disp + dispatch_scratch_bytes(d->T, d->E), kAlign);
-  l.gate = align_up(l.idx + Tk * 4, kAlign);
-  l.offsets = align_up(l.gate + Tk * 4, kAlign);
-  l.row_of = align_up(l.offsets + (static_cast<size_t>(d->E) + 1) * 4, kAlign);
-  l.src = align_up(l.row_of + Tk * 4, kAlign);
-  l.xperm = align_up(l.src + Tk * 4, kAlign);
-  l.act = align_up(l.xperm + Tk * d->head_dim * 2, kAlign);
+  l.idx = align_up(l.disp + H * dispatch_scratch_bytes(d->T, d->E), kAlign);
+  l.gate = align_up(l.idx + H * Tk * 4, kAlign);
+  l.offsets = align_up(l.gate + H * Tk * 4, kAlign);
+  l.row_of = align_up(l.offsets + H * (static_cast<size_t>(d->E) + 1) * 4, kAlign);
+  l.src = align_up(l.row_of + H * Tk * 4, kAlign);
+  l.xperm = align_up(l.src + H * Tk * 4, kAlign);
+  l.act = align_up(l.xperm + H * Tk * d->head_dim * 2, kAlign);
   l.end = align_up(l.act + Tk * d->inter * 2, kAlign);
   return l;
 }
@@ -104,64 +108,66 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
   const int H = dims->n_heads, Dh = dims->head_dim, E = dims->E, I = dims->inter, k = dims->top_k;
   const int64_t T = dims->T, Tk = T * k;
   int* status = static_cast<int*>(ws);
-  const int64_t nblk_e = static_cast<int64_t>(dispatch_scratch_bytes(T, E) / 8);
+  int32_t* idx = topk_idx != nullptr ? topk_idx : at<int32_t>(ws, l.idx);
+  float* gate = at<float>(ws, l.gate);
+
+  // 1. every head's router in one batched GEMM (fused top-k)
+  rc = launch_router_headlocal(x, T, dims->d, H, Dh, w_router, E, k, bias, idx, gate, logits, status, sms, s);
+  if (rc != MOE_OK) return rc;
+
+  // 2. every head's sort and gather in one set of launches
+  DispatchArgs da{};
+  da.x = x;
+  da.x_ld = dims->d;
+  da.x_head_off = Dh;
+  da.heads = H;
+  da.topk_idx = idx;
+  da.T = T;
+  da.d = Dh;
+  da.k = k;
+  da.E = E;
+  da.offsets = at<int32_t>(ws, l.offsets);
+  da.row_of = at<int32_t>(ws, l.row_of);
+  da.src_token = at<int32_t>(ws, l.src);
+  da.x_perm = at<uint16_t>(ws, l.xperm);
+  da.block_counts = at<int32_t>(ws, l.disp);
+  da.block_base = at<int32_t>(ws, l.disp) + static_cast<int64_t>(H) * dispatch_counter_cells(T, E);
+  da.status = status;
+  da.sm_count = sms;
+  if ((rc = launch_dispatch(da, s)) != MOE_OK) return rc;
+
+  // 3. each head's grouped expert GEMMs (y_perm overwrites the head's x_perm)
   for (int j = 0; j < H; ++j) {
-    const moe_bf16* xj = x + static_cast<int64_t>(j) * Dh;
-    int32_t* idx = topk_idx != nullptr ? topk_idx + static_cast<int64_t>(j) * Tk : at<int32_t>(ws, l.idx);
-    float* gate = at<float>(ws, l.gate);
-    float* lg = logits != nullptr ? logits + static_cast<int64_t>(j) * T * E : nullptr;
-    rc = launch_router_head(xj, dims->d, w_router + static_cast<int64_t>(j) * E * Dh,
-                            bias != nullptr ? bias + static_cast<int64_t>(j) * E : nullptr, T, Dh, E, k, idx, gate, lg,
-                            status, sms, s);
-    if (rc != MOE_OK) return rc;
-
-    DispatchArgs da{};
-    da.x = xj;
-    da.x_ld = dims->d;
-    da.topk_idx = idx;
-    da.T = T;
-    da.d = Dh;
-    da.k = k;
-    da.E = E;
-    da.offsets = at<int32_t>(ws, l.offsets);
-    da.row_of = at<int32_t>(ws, l.row_of);
-    da.src_token = at<int32_t>(ws, l.src);
-    da.x_perm = at<uint16_t>(ws, l.xperm);
-    da.block_counts = at<int32_t>(ws, l.disp);
-    da.block_base = at<int32_t>(ws, l.disp) + nblk_e;
-    da.status = status;
-    da.sm_count = sms;
-    if ((rc = launch_dispatch(da, s)) != MOE_OK) return rc;
-
     FfnArgs fa{};
-    fa.offsets = da.offsets;
+    fa.offsets = da.offsets + static_cast<int64_t>(j) * (E + 1);
     fa.rows = Tk;
     fa.d = Dh;
     fa.I = I;
     fa.E = E;
     fa.status = status;
     fa.sm_count = sms;
-    fa.x_perm = da.x_perm;
+    fa.x_perm = da.x_perm + static_cast<int64_t>(j) * Tk * Dh;
     fa.w13 = w13 + static_cast<int64_t>(j) * E * 2 * I * Dh;
     fa.act = at<uint16_t>(ws, l.act);
     if ((rc = launch_gemm1(fa, s)) != MOE_OK) return rc;
     fa.w_down = w_down + static_cast<int64_t>(j) * E * Dh * I;
-    fa.y_perm = da.x_perm;  // x_perm is dead after GEMM-1
+    fa.y_perm = da.x_perm + static_cast<int64_t>(j) * Tk * Dh;
     if ((rc = launch_gemm2(fa, s)) != MOE_OK) return rc;
-
-    CombineArgs ca{};
-    ca.y_perm = fa.y_perm;
-    ca.row_of = da.row_of;
-    ca.gate = gate;
-    ca.out = out + static_cast<int64_t>(j) * Dh;
-    ca.out_ld = dims->d;
-    ca.T = T;
-    ca.d = Dh;
-    ca.k = k;
-    ca.sm_count = sms;
-    if ((rc = launch_combine(ca, s)) != MOE_OK) return rc;
   }
-  return MOE_OK;
+
+  // 4. every head's combine into its columns of out, one launch
+  CombineArgs ca{};
+  ca.y_perm = da.x_perm;
+  ca.row_of = da.row_of;
+  ca.gate = gate;
+  ca.out = out;
+  ca.out_ld = dims->d;
+  ca.heads = H;
+  ca.T = T;
+  ca.d = Dh;
+  ca.k = k;
+  ca.sm_count = sms;
+  return launch_combine(ca, s);
 }
 
 }  // extern "C"

@@ -20,6 +20,12 @@ struct DispatchArgs {
   int32_t* src_token;
   uint16_t* x_perm;        // nullptr: permutation only
   int64_t x_ld;            // row stride of x in elements (0: d)
+  // Independent sorts side by side (head-local layer): head h reads x's
+  // columns from h * x_head_off and topk_idx[h], writes offsets[h], row_of[h],
+  // src_token[h], x_perm[h] (each the single-sort size) and uses its own
+  // block counters.  heads <= 1: one sort.
+  int heads;
+  int64_t x_head_off;
   int32_t* block_counts;   // scratch [nblk * E]
   int32_t* block_base;     // scratch [nblk * E]
   int* status;
@@ -76,11 +82,15 @@ struct CombineArgs {
   int64_t T;
   int d, k;
   int64_t out_ld;          // row stride of out in elements (0: d)
+  // Independent combines side by side: head h reads y_perm[h], row_of[h],
+  // gate[h] and writes out's columns from h * d (heads <= 1: one combine).
+  int heads;
   int sm_count;
 };
 
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 size_t dispatch_scratch_bytes(int64_t T, int E);
+size_t dispatch_counter_cells(int64_t T, int E);  // ceil(T / block) * E: one of the two counter arrays
 int launch_route(const RouteArgs& a, cudaStream_t stream);
 int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream);
 bool route_fused_supported(int head_dim);
@@ -100,10 +110,10 @@ int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w
 bool make_tmap_bf16_2d(void* tmap /* CUtensorMap* */, const void* base, uint64_t cols, uint64_t rows,
                        uint32_t box_cols, uint32_t box_rows, uint64_t row_stride_elems = 0);
 
-// Head-local router for one head: s = x_j W_router[j]^T + b[j] over the strided
-// head view of x, with the fused top-k epilogue (idx/gate [T, k]).
-int launch_router_head(const uint16_t* x_head, int64_t x_ld, const uint16_t* w_router_head, const float* bias_head,
-                       int64_t T, int head_dim, int E, int k, int32_t* idx, float* gate, float* logits, int* status,
-                       int sm_count, cudaStream_t stream);
+int launch_router_headlocal(const uint16_t* x, int64_t T, int d, int H, int Dh, const uint16_t* w_router, int E,
+                            int k, const float* bias, int32_t* idx, float* gate, float* logits, int* status,
+                            int sm_count, cudaStream_t stream);
+
+
 
 }  // namespace moe
