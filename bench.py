@@ -287,8 +287,8 @@ def measure_headlocal_variant(torch, moe, steps: int) -> dict:
     flops = cfg.T * cfg.n_heads * (2 * cfg.head_dim * cfg.E + 6 * cfg.top_k * cfg.head_dim * cfg.inter)
     return {"workload": cfg.note, "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "layer_tflops": flops / (ms * 1e-3) / 1e12,
-            "path": "moe_forward_headlocal: per head, router GEMM + top-k, sort, grouped SwiGLU GEMMs, combine "
-                    "into the head's columns; heads in sequence on one stream"}
+            "path": "moe_forward_headlocal: all heads' routers + top-k as one batched GEMM, one sort and gather "
+                    "over (head, token), grouped SwiGLU GEMMs head by head, one combine into each head's columns"}
 
 
 def measure_ext_variant(torch, moe, steps: int) -> dict:

@@ -2,8 +2,10 @@
 // workspace layout and the order of the stages on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "moe.h"
@@ -75,6 +77,105 @@ T* at(void* ws, size_t off) {
 
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
 
+// moe_forward_host runs the layer over token chunks of ceil(T / n) tokens,
+// n = min(ceil(T / 8192), 8).  x comes in on one stream and out goes back on
+// another, so while chunk i computes on the caller's stream the copy engines
+// bring chunk i+1 in and take chunk i-1 out.  Routing, each expert row and the
+// combine are per token, so every token gets the same bits as in a single
+// moe_forward over the whole batch.
+constexpr int kHostChunksMax = 8;
+constexpr int64_t kHostChunkMinTokens = 8192;
+constexpr int kMaxDevices = 64;
+
+int host_chunks(int64_t T) {
+  return static_cast<int>(std::min<int64_t>(std::max<int64_t>((T + kHostChunkMinTokens - 1) / kHostChunkMinTokens, 1),
+                                            kHostChunksMax));
+}
+
+int64_t host_chunk_tokens(int64_t T) {
+  const int64_t n = host_chunks(T);
+  return (T + n - 1) / n;
+}
+
+// Copy streams and events of one device, created on first use and kept for
+// the life of the process.  `mu` serialises moe_forward_host calls on the
+// device (each call ends with all three streams drained).
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, out_end = nullptr;
+  cudaEvent_t in_done[kHostChunksMax] = {}, fwd_done[kHostChunksMax] = {};
+};
+
+HostPipe g_host_pipe[kMaxDevices];
+
+void host_pipe_release(HostPipe& p) {
+  if (p.in) cudaStreamDestroy(p.in);
+  if (p.out) cudaStreamDestroy(p.out);
+  if (p.start) cudaEventDestroy(p.start);
+  if (p.out_end) cudaEventDestroy(p.out_end);
+  for (int i = 0; i < kHostChunksMax; ++i) {
+    if (p.in_done[i]) cudaEventDestroy(p.in_done[i]);
+    if (p.fwd_done[i]) cudaEventDestroy(p.fwd_done[i]);
+    p.in_done[i] = p.fwd_done[i] = nullptr;
+  }
+  p.in = p.out = nullptr;
+  p.start = p.out_end = nullptr;
+}
+
+// Caller holds p.mu.
+bool host_pipe_ready(HostPipe& p) {
+  if (p.ready) return true;
+  auto ev = [](cudaEvent_t* e) { return cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
+  bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess && ev(&p.start) &&
+            ev(&p.out_end);
+  for (int i = 0; ok && i < kHostChunksMax; ++i) ok = ev(&p.in_done[i]) && ev(&p.fwd_done[i]);
+  if (!ok) {
+    host_pipe_release(p);
+    return false;
+  }
+  p.ready = true;
+  return true;
+}
+
+// The whole layer on device buffers.  The host-buffer path clears the device
+// status word once and runs its chunks with clear_status = false, so the
+// word collects the flags of every chunk.
+int forward_impl(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws,
+                 size_t ws_bytes, void* stream, bool clear_status) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
+      out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(w13) || !aligned16(w_down) ||
+      !aligned16(out) || !aligned16(ws) || (bias != nullptr && !aligned16(bias)))
+    return MOE_ERR_MISALIGNED;
+  const ForwardLayout f = forward_layout(dims);
+  if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (clear_status && (rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
+  int32_t* idx = at<int32_t>(ws, f.idx);
+  float* gate = at<float>(ws, f.gate);
+  int32_t* offsets = at<int32_t>(ws, f.offsets);
+  int32_t* row_of = at<int32_t>(ws, f.row_of);
+  int32_t* src = at<int32_t>(ws, f.src);
+  moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
+  moe_bf16* act = at<moe_bf16>(ws, f.act);
+  // y_perm reuses x_perm's memory: x_perm is dead once expert GEMM-1 has run.
+  // (moe_expert_gemm1_gather would skip x_perm entirely, but on B300 its
+  // four-row TMA gathers are issue-bound and GEMM-1 runs ~3x slower, more
+  // than the ~1.2 ms the separate gather costs on the clip workload.)
+  moe_bf16* yperm = xperm;
+  if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm1(dims, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  return moe_combine(dims, yperm, row_of, gate, out, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -125,11 +226,13 @@ int moe_workspace_size(const moe_dims* dims, size_t* bytes) {
 }
 
 int moe_workspace_size_host(const moe_dims* dims, size_t* bytes) {
-  size_t b = 0;
-  const int rc = moe_workspace_size(dims, &b);
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  const int rc = moe_check_dims(dims);
   if (rc != MOE_OK) return rc;
+  moe_dims chunk = *dims;
+  chunk.T = host_chunk_tokens(dims->T);
   const size_t io = align_up(static_cast<size_t>(dims->T) * dims->d * 2, kAlign);
-  *bytes = b + 2 * io;
+  *bytes = forward_layout(&chunk).end + 2 * io;
   return MOE_OK;
 }
 
@@ -451,34 +554,7 @@ int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row
 int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws,
                 size_t ws_bytes, void* stream) {
-  int rc = moe_check_dims(dims);
-  if (rc != MOE_OK) return rc;
-  if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
-      out == nullptr || ws == nullptr)
-    return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(w13) || !aligned16(w_down) ||
-      !aligned16(out) || !aligned16(ws) || (bias != nullptr && !aligned16(bias)))
-    return MOE_ERR_MISALIGNED;
-  const ForwardLayout f = forward_layout(dims);
-  if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
-  int32_t* idx = at<int32_t>(ws, f.idx);
-  float* gate = at<float>(ws, f.gate);
-  int32_t* offsets = at<int32_t>(ws, f.offsets);
-  int32_t* row_of = at<int32_t>(ws, f.row_of);
-  int32_t* src = at<int32_t>(ws, f.src);
-  moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
-  moe_bf16* act = at<moe_bf16>(ws, f.act);
-  // y_perm reuses x_perm's memory: x_perm is dead once expert GEMM-1 has run.
-  // (moe_expert_gemm1_gather would skip x_perm entirely, but on B300 its
-  // four-row TMA gathers are issue-bound and GEMM-1 runs ~3x slower, more
-  // than the ~1.2 ms the separate gather costs on the clip workload.)
-  moe_bf16* yperm = xperm;
-  if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
-  if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
-  if ((rc = moe_expert_gemm1(dims, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
-  if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
-  return moe_combine(dims, yperm, row_of, gate, out, stream);
+  return forward_impl(dims, x, w_lat, w_head, bias, w13, w_down, out, ws, ws_bytes, stream, true);
 }
 
 int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
@@ -630,21 +706,63 @@ int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf1
                      size_t ws_bytes, void* stream) {
   int rc = moe_check_dims(dims);
   if (rc != MOE_OK) return rc;
-  if (x_host == nullptr || out_host == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
-  size_t need = 0, inner = 0;
-  moe_workspace_size_host(dims, &need);
-  moe_workspace_size(dims, &inner);
+  if (x_host == nullptr || out_host == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr ||
+      w_down == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_lat) || !aligned16(w_head) || !aligned16(w13) || !aligned16(w_down) || !aligned16(ws) ||
+      (bias != nullptr && !aligned16(bias)))
+    return MOE_ERR_MISALIGNED;
+  size_t need = 0;
+  if ((rc = moe_workspace_size_host(dims, &need)) != MOE_OK) return rc;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  const size_t io_bytes = static_cast<size_t>(dims->T) * dims->d * 2;
-  const size_t io = align_up(io_bytes, kAlign);
+  const int64_t T = dims->T, tc = host_chunk_tokens(T);
+  const int n = host_chunks(T);
+  const size_t row = static_cast<size_t>(dims->d);  // elements per token
+  moe_dims cd = *dims;
+  cd.T = tc;
+  const size_t inner = forward_layout(&cd).end;
+  const size_t io = align_up(static_cast<size_t>(T) * row * 2, kAlign);
   moe_bf16* x_dev = at<moe_bf16>(ws, inner);
   moe_bf16* out_dev = at<moe_bf16>(ws, inner + io);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  HostPipe& p = g_host_pipe[dev];
+  std::lock_guard<std::mutex> lock(p.mu);
+  if (!host_pipe_ready(p)) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(x_dev, x_host, io_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((rc = moe_forward(dims, x_dev, w_lat, w_head, bias, w13, w_down, out_dev, ws, inner, stream)) != MOE_OK)
-    return rc;
-  if (cudaMemcpyAsync(out_host, out_dev, io_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
-  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // The copies wait for the work already queued on the caller's stream.
+  bool good = ok(cudaEventRecord(p.start, s)) && ok(cudaStreamWaitEvent(p.in, p.start, 0)) &&
+              ok(cudaStreamWaitEvent(p.out, p.start, 0));
+  for (int i = 0; good && i < n; ++i) {
+    const int64_t t0 = i * tc, ti = std::min(tc, T - t0);
+    if (ti <= 0) break;
+    good = ok(cudaMemcpyAsync(x_dev + t0 * row, x_host + t0 * row, static_cast<size_t>(ti) * row * 2,
+                              cudaMemcpyHostToDevice, p.in)) &&
+           ok(cudaEventRecord(p.in_done[i], p.in));
+  }
+  if (good) rc = moe_clear_device_status(ws, stream);
+  for (int i = 0; good && rc == MOE_OK && i < n; ++i) {
+    const int64_t t0 = i * tc, ti = std::min(tc, T - t0);
+    if (ti <= 0) break;
+    cd.T = ti;
+    good = ok(cudaStreamWaitEvent(s, p.in_done[i], 0));
+    if (good)
+      rc = forward_impl(&cd, x_dev + t0 * row, w_lat, w_head, bias, w13, w_down, out_dev + t0 * row, ws, inner,
+                        stream, false);
+    if (good && rc == MOE_OK)
+      good = ok(cudaEventRecord(p.fwd_done[i], s)) && ok(cudaStreamWaitEvent(p.out, p.fwd_done[i], 0)) &&
+             ok(cudaMemcpyAsync(out_host + t0 * row, out_dev + t0 * row, static_cast<size_t>(ti) * row * 2,
+                                cudaMemcpyDeviceToHost, p.out));
+  }
+  if (good) good = ok(cudaEventRecord(p.out_end, p.out)) && ok(cudaStreamWaitEvent(s, p.out_end, 0));
+  // Drain all three streams, after an error too, so that no copy still uses
+  // the host buffers once this returns.
+  const bool in_ok = ok(cudaStreamSynchronize(p.in));
+  const bool out_ok = ok(cudaStreamSynchronize(p.out));
+  const bool s_ok = ok(cudaStreamSynchronize(s));
+  if (rc != MOE_OK) return rc;
+  return good && in_ok && out_ok && s_ok ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -101,8 +101,9 @@ int moe_scratch_size(const moe_dims* dims, size_t* bytes);
  * y_perm).  Any buffer of this size also serves every stage call. */
 int moe_workspace_size(const moe_dims* dims, size_t* bytes);
 
-/* Bytes of workspace needed by moe_forward_host: moe_workspace_size plus
- * device staging for x and out. */
+/* Bytes of workspace needed by moe_forward_host: moe_workspace_size for one
+ * token chunk of that call (see moe_forward_host) plus device staging for
+ * the whole x and out. */
 int moe_workspace_size_host(const moe_dims* dims, size_t* bytes);
 
 /* Zeroes the sticky device status word in `ws` (enqueued on `stream`). */
@@ -330,7 +331,9 @@ int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x,
  *   topk_idx [n_heads, T, top_k] int32 or NULL (written: each head's choice)
  *   logits [n_heads, T, E] fp32 or NULL (written: each head's scores)
  * Rules: head_dim % 64 == 0, inter % 64 == 0, E <= 256, top_k <= min(8, E).
- * The heads run in sequence on `stream`, reusing one set of buffers. */
+ * All heads' routers run as one batched GEMM, their sorts, gathers and
+ * combines as single launches over (head, token); the expert GEMMs run head
+ * by head on `stream`, each head in its own slice of the workspace. */
 int moe_workspace_size_headlocal(const moe_dims* dims, size_t* bytes);
 int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
                                   void* stream);
@@ -338,11 +341,18 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
                           const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx,
                           float* logits, void* ws, size_t ws_bytes, void* stream);
 
-/* moe_forward for a caller whose activations live in host memory: copies
- * x_host [T, d] to the device, runs the layer, copies out to out_host [T, d]
- * and synchronises `stream`.  Weights are device pointers.  Host buffers
- * should be page-locked for full copy bandwidth.  ws: at least
- * moe_workspace_size_host bytes. */
+/* moe_forward for a caller whose activations live in host memory: x_host
+ * [T, d] in, out_host [T, d] out, weights on the device; returns after the
+ * result is in out_host (the call synchronises `stream`).  The layer runs
+ * over n = min(ceil(T / 8192), 8) token chunks of ceil(T / n) tokens: the
+ * chunks' copies to the device run on one internal stream and the copies
+ * back on another, overlapping the compute of the neighbouring chunks on
+ * `stream`.  Each token's result has the same bits as moe_forward over the
+ * whole batch.  The device status word at the start of ws collects the flags
+ * of every chunk.  Host buffers should be page-locked: pageable memory still
+ * gives correct results, but the copies then serialise with the compute.
+ * Calls for the same device are serialised by an internal lock.  ws: at
+ * least moe_workspace_size_host bytes. */
 int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* w_lat,
                      const moe_bf16* w_head, const float* bias, const moe_bf16* w13,
                      const moe_bf16* w_down, moe_bf16* out_host, void* ws, size_t ws_bytes,

@@ -57,9 +57,21 @@ def test_workspace_sizes(L):
     Tk = 107520 * 6
     assert s >= 107520 * 6144 * 2
     assert w >= s + Tk * 4096 * 2 + Tk * 1024 * 2 + 4 * Tk * 4
-    assert h >= w + 2 * 107520 * 4096 * 2
     with pytest.raises(moe.MoeError):
         moe.moe_workspace_size(moe.moe_dims.make(0, 4096, 128, 1024))
+
+
+@pytest.mark.parametrize("T,chunk", [(1, 1), (8192, 8192), (8193, 4097), (20000, 6667), (65536, 8192),
+                                     (65537, 8193), (107520, 13440)])
+def test_host_workspace_is_one_chunk_plus_staging(L, T, chunk):
+    # moe_forward_host runs n = min(ceil(T / 8192), 8) chunks of ceil(T / n)
+    # tokens: its workspace is one chunk's forward workspace plus x and out
+    # staging for the whole batch (each rounded up to 1 KiB).
+    d = 4096
+    h = moe.moe_workspace_size_host(moe.moe_dims.make(T, d, 128, 1024))
+    inner = moe.moe_workspace_size(moe.moe_dims.make(chunk, d, 128, 1024))
+    io = -(-T * d * 2 // 1024) * 1024
+    assert h == inner + 2 * io
 
 
 def test_null_and_misaligned_pointers_are_rejected_on_the_host(L):

@@ -78,6 +78,30 @@ def test_forward_host_buffers():
     assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("T,pinned", [(8193, True), (20000, True), (9000, False)])
+def test_forward_host_chunks_match_one_forward(T, pinned):
+    # 2 or 3 token chunks with a ragged last one, copies overlapping compute
+    # (pinned) or serialised with it (pageable): the same bits as one
+    # moe_forward over the whole batch, and the oracle on tokens of every chunk
+    inp = G.small_inputs(T=T, d=512, E=32, inter=128, seed=3)
+    dev = G.Dev(inp)
+    ref = dev.forward()
+    idx, _, _ = dev.route(want_logits=False)
+    assert dev.status() == 0
+    ws = moe.alloc_workspace(moe.moe_workspace_size_host(dev.dims))
+    xh = dev.x.cpu()
+    oh = torch.full_like(xh, float("nan"))
+    if pinned:
+        xh, oh = xh.pin_memory(), oh.pin_memory()
+    moe.moe_forward_host(dev.dims, xh, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, oh, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
+    rng = np.random.default_rng(T)
+    tok = np.unique(np.r_[0, T - 1, T // 2, rng.choice(T, 120, replace=False)])
+    want = O.forward_bits(inp, tokens=tok, topk_idx=idx.cpu().numpy()[tok])
+    G.check_out(G.host_f64(oh[tok]), want["out"])
+
+
 @pytest.mark.parametrize("kw", [dict(T=3000, d=512, E=32, inter=256), dict(T=77, d=4096, E=8, inter=1024),
                                 dict(T=1, d=512, E=16, inter=128)])
 def test_gathered_gemm1_equals_gemm1_on_x_perm(kw):
