@@ -37,7 +37,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // Writes this warp's 32 rows x 64 bf16 columns (p[j] = columns 2j, 2j+1 of
 // this thread's row) to the output at (row0w, col0).  nvalid = rows of the 32
 // that may be written; row_ptr = this thread's row at col0 (fallback path).
-__device__ __forceinline__ void store_rows64(EpiCtx& ctx, int row0w, int col0, int nvalid, const uint32_t (&p)[32],
+__device__ __forceinline__ void store_rows64(EpiCtx& ctx, int row0w, int col0, int nvalid, const uint32_t* p,
                                              uint16_t* row_ptr) {
   if (nvalid >= 32) {
     if (ctx.pending) {  // the previous bulk store must be done reading the chunk
@@ -64,6 +64,15 @@ __device__ __forceinline__ void store_rows64(EpiCtx& ctx, int row0w, int col0, i
   }
 }
 
+// Hands the accumulator back to the MMA warp.  The caller's tcgen05.ld's have
+// completed (tmem_ld32 waits on them), so the next tile's MMAs may overwrite
+// the columns while this warp's stores of the tile are still under way.
+__device__ __forceinline__ void release_accumulator(EpiCtx& ctx) {
+  ptx::tc_fence_before();
+  ptx::mbar_arrive(ctx.tempty);
+  ctx.released = true;
+}
+
 __device__ __forceinline__ int warp_valid_rows(const TileCoord& c, const EpiCtx& ctx) {
   const int first = c.row0 + ctx.quad * 32;
   const int n = c.row_end - first;
@@ -71,6 +80,9 @@ __device__ __forceinline__ int warp_valid_rows(const TileCoord& c, const EpiCtx&
 }
 
 // out[row, n_blk*BN + j] = bf16(acc[j])  (expert GEMM-2: y_perm)
+// The row's BN/2 packed bf16 pairs are read out of TMEM first and the
+// accumulator released, so the MMAs of a later tile do not wait for the
+// bulk stores of this one.
 struct EpiStoreBf16 {
   struct Params {
     uint16_t* out;
@@ -82,26 +94,28 @@ struct EpiStoreBf16 {
     const int nvalid = warp_valid_rows(c, ctx);
     const int row = c.row0 + r;
     uint16_t* row_ptr = p.out + static_cast<int64_t>(row) * p.ld + c.n_blk * BN;
-#pragma unroll 1
-    for (int col = 0; col < BN; col += 64) {
-      uint32_t pk[32];
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int col = 0; col < BN; col += 32) {
       float v[32];
       __syncwarp();
       tmem_ld32(taddr + col, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-      __syncwarp();
-      tmem_ld32(taddr + col + 32, v);
+      for (int j = 0; j < 16; ++j) pk[col / 2 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    }
+    release_accumulator(ctx);
+    if (nvalid > 0) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) pk[16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-      if (nvalid > 0) store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * BN + col, nvalid, pk, row_ptr + col);
+      for (int col = 0; col < BN; col += 64)
+        store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * BN + col, nvalid, pk + col / 2, row_ptr + col);
     }
   }
 };
 
 // Expert GEMM-1 with fused SwiGLU.  The B operand is the interleaved w13:
 // within every 128 output columns, 64 gate rows then the matching 64 up rows.
-// act[row, n_blk*BN/2 + 64*j + i] = bf16(silu(g) * u).
+// act[row, n_blk*BN/2 + 64*j + i] = bf16(silu(g) * u).  All of the row's
+// activations are formed in registers before the accumulator is released.
 struct EpiSwiGLU {
   struct Params {
     uint16_t* act;
@@ -114,9 +128,9 @@ struct EpiSwiGLU {
     const int nvalid = warp_valid_rows(c, ctx);
     const int row = c.row0 + r;
     uint16_t* row_ptr = p.act + static_cast<int64_t>(row) * p.ld + c.n_blk * (BN / 2);
-#pragma unroll 1
+    uint32_t pk[BN / 4];
+#pragma unroll
     for (int j = 0; j < BN / 128; ++j) {
-      uint32_t pk[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float g[32], u[32];
@@ -127,11 +141,16 @@ struct EpiSwiGLU {
         for (int i = 0; i < 16; ++i) {
           const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
           const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
-          pk[h * 16 + i] = pack_bf16x2(a0, a1);
+          pk[j * 32 + h * 16 + i] = pack_bf16x2(a0, a1);
         }
       }
-      if (nvalid > 0)
-        store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * (BN / 2) + j * 64, nvalid, pk, row_ptr + j * 64);
+    }
+    release_accumulator(ctx);
+    if (nvalid > 0) {
+#pragma unroll
+      for (int j = 0; j < BN / 128; ++j)
+        store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * (BN / 2) + j * 64, nvalid, pk + j * 32,
+                     row_ptr + j * 64);
     }
   }
 };

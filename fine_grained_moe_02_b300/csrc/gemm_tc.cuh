@@ -95,6 +95,8 @@ struct EpiCtx {
   int lane;
   int quad;         // TMEM lane quadrant = rows [32*quad, 32*quad + 32) of the tile
   bool pending;     // lane 0 has a committed bulk store that may still read `stage`
+  uint32_t tempty;  // shared address of the current accumulator's "empty" barrier
+  bool released;    // this warp has already arrived on `tempty` for the current tile
 };
 
 struct TileCoord {
@@ -384,7 +386,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    EpiCtx ctx{&tmap_d, ptx::smem_u32(smem + STAGES * S::kStageBytes + quad * kOutChunkBytes), lane, quad, false};
+    EpiCtx ctx{&tmap_d, ptx::smem_u32(smem + STAGES * S::kStageBytes + quad * kOutChunkBytes), lane, quad, false,
+               0u, false};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = first_tile; tile < total; tile += tile_step) {
@@ -396,9 +399,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       }
       ptx::tc_fence_after();
       const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles, CL, crank);
+      ctx.tempty = ptx::smem_u32(&tempty_bar[acc]);
+      ctx.released = false;
+      // an epilogue may hand the accumulator back itself (release_accumulator)
+      // as soon as it holds the tile in registers, before its stores
       Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile, ctx);
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_u32(&tempty_bar[acc]));
+      if (!ctx.released) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ctx.tempty);
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     // bulk stores read shared memory and write global memory asynchronously:
