@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -39,8 +40,9 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
   // the stage byte count and the shared-memory ring would disagree
   if (b_box_rows != BN / CL) return MOE_ERR_UNSUPPORTED_SHAPE;
   auto kern = gemm_tc_kernel<BN, Epi, CL>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kDynBytes) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  // once per device: later calls (and stream captures) launch without it
+  static std::atomic<uint64_t> smem_set{0};
+  if (!smem_attr_ready(kern, S::kDynBytes, smem_set)) return MOE_ERR_CUDA;
   if (grid < 1) grid = 1;
   if constexpr (CL == 1) {
     kern<<<grid, kGemmThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);

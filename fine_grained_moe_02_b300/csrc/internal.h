@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -9,6 +11,20 @@ namespace moe {
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
+
+// Raises a kernel's dynamic shared-memory limit on the current device the
+// first time it is launched there; `done` (one per kernel) holds one bit per
+// device.  Later launches, stream captures included, skip the call.
+template <class Kern>
+inline bool smem_attr_ready(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
 
 struct DispatchArgs {
   const uint16_t* x;

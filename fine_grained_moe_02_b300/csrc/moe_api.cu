@@ -80,10 +80,14 @@ int* status_ptr(void* ws) { return static_cast<int*>(ws); }
 // moe_forward_host runs the layer over token chunks of ceil(T / n) tokens,
 // n = min(ceil(T / 8192), 8).  x comes in on one stream and out goes back on
 // another, so while chunk i computes on the caller's stream the copy engines
-// bring chunk i+1 in and take chunk i-1 out.  Routing, each expert row and the
-// combine are per token, so every token gets the same bits as in a single
-// moe_forward over the whole batch.
+// bring chunk i+1 in and take chunk i-1 out.  With n >= 3 the first and the
+// last chunk are each cut 1:3, the short piece at the end of the batch, so
+// the copy in before the first compute and the compute and copy out after the
+// last copy in are short.  Routing, each expert row and the combine are per
+// token, so every token gets the same bits as in a single moe_forward over
+// the whole batch.
 constexpr int kHostChunksMax = 8;
+constexpr int kHostPiecesMax = kHostChunksMax + 2;
 constexpr int64_t kHostChunkMinTokens = 8192;
 constexpr int kMaxDevices = 64;
 
@@ -97,6 +101,29 @@ int64_t host_chunk_tokens(int64_t T) {
   return (T + n - 1) / n;
 }
 
+// The pieces the layer runs over, in token order; returns their count.
+int host_pieces(int64_t T, int64_t* start, int64_t* len) {
+  const int n = host_chunks(T);
+  const int64_t tc = host_chunk_tokens(T);
+  int m = 0;
+  int64_t t0 = 0;
+  for (int i = 0; i < n && t0 < T; ++i) {
+    const int64_t ti = std::min(tc, T - t0);
+    if (n >= 3 && (i == 0 || i == n - 1) && ti >= 4) {
+      const int64_t a = (i == 0) ? ti / 4 : ti - ti / 4;
+      start[m] = t0;
+      len[m++] = a;
+      start[m] = t0 + a;
+      len[m++] = ti - a;
+    } else {
+      start[m] = t0;
+      len[m++] = ti;
+    }
+    t0 += ti;
+  }
+  return m;
+}
+
 // Copy streams and events of one device, created on first use and kept for
 // the life of the process.  `mu` serialises moe_forward_host calls on the
 // device (each call ends with all three streams drained).
@@ -105,7 +132,7 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, out_end = nullptr;
-  cudaEvent_t in_done[kHostChunksMax] = {}, fwd_done[kHostChunksMax] = {};
+  cudaEvent_t in_done[kHostPiecesMax] = {}, fwd_done[kHostPiecesMax] = {};
 };
 
 HostPipe g_host_pipe[kMaxDevices];
@@ -115,7 +142,7 @@ void host_pipe_release(HostPipe& p) {
   if (p.out) cudaStreamDestroy(p.out);
   if (p.start) cudaEventDestroy(p.start);
   if (p.out_end) cudaEventDestroy(p.out_end);
-  for (int i = 0; i < kHostChunksMax; ++i) {
+  for (int i = 0; i < kHostPiecesMax; ++i) {
     if (p.in_done[i]) cudaEventDestroy(p.in_done[i]);
     if (p.fwd_done[i]) cudaEventDestroy(p.fwd_done[i]);
     p.in_done[i] = p.fwd_done[i] = nullptr;
@@ -131,7 +158,7 @@ bool host_pipe_ready(HostPipe& p) {
   bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess && ev(&p.start) &&
             ev(&p.out_end);
-  for (int i = 0; ok && i < kHostChunksMax; ++i) ok = ev(&p.in_done[i]) && ev(&p.fwd_done[i]);
+  for (int i = 0; ok && i < kHostPiecesMax; ++i) ok = ev(&p.in_done[i]) && ev(&p.fwd_done[i]);
   if (!ok) {
     host_pipe_release(p);
     return false;
@@ -716,7 +743,8 @@ int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf1
   if ((rc = moe_workspace_size_host(dims, &need)) != MOE_OK) return rc;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int64_t T = dims->T, tc = host_chunk_tokens(T);
-  const int n = host_chunks(T);
+  int64_t p_start[kHostPiecesMax], p_len[kHostPiecesMax];
+  const int n = host_pieces(T, p_start, p_len);
   const size_t row = static_cast<size_t>(dims->d);  // elements per token
   moe_dims cd = *dims;
   cd.T = tc;
@@ -735,25 +763,20 @@ int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf1
   bool good = ok(cudaEventRecord(p.start, s)) && ok(cudaStreamWaitEvent(p.in, p.start, 0)) &&
               ok(cudaStreamWaitEvent(p.out, p.start, 0));
   for (int i = 0; good && i < n; ++i) {
-    const int64_t t0 = i * tc, ti = std::min(tc, T - t0);
-    if (ti <= 0) break;
-    good = ok(cudaMemcpyAsync(x_dev + t0 * row, x_host + t0 * row, static_cast<size_t>(ti) * row * 2,
-                              cudaMemcpyHostToDevice, p.in)) &&
+    const size_t off = static_cast<size_t>(p_start[i]) * row, bytes = static_cast<size_t>(p_len[i]) * row * 2;
+    good = ok(cudaMemcpyAsync(x_dev + off, x_host + off, bytes, cudaMemcpyHostToDevice, p.in)) &&
            ok(cudaEventRecord(p.in_done[i], p.in));
   }
   if (good) rc = moe_clear_device_status(ws, stream);
   for (int i = 0; good && rc == MOE_OK && i < n; ++i) {
-    const int64_t t0 = i * tc, ti = std::min(tc, T - t0);
-    if (ti <= 0) break;
-    cd.T = ti;
+    const size_t off = static_cast<size_t>(p_start[i]) * row, bytes = static_cast<size_t>(p_len[i]) * row * 2;
+    cd.T = p_len[i];
     good = ok(cudaStreamWaitEvent(s, p.in_done[i], 0));
     if (good)
-      rc = forward_impl(&cd, x_dev + t0 * row, w_lat, w_head, bias, w13, w_down, out_dev + t0 * row, ws, inner,
-                        stream, false);
+      rc = forward_impl(&cd, x_dev + off, w_lat, w_head, bias, w13, w_down, out_dev + off, ws, inner, stream, false);
     if (good && rc == MOE_OK)
       good = ok(cudaEventRecord(p.fwd_done[i], s)) && ok(cudaStreamWaitEvent(p.out, p.fwd_done[i], 0)) &&
-             ok(cudaMemcpyAsync(out_host + t0 * row, out_dev + t0 * row, static_cast<size_t>(ti) * row * 2,
-                                cudaMemcpyDeviceToHost, p.out));
+             ok(cudaMemcpyAsync(out_host + off, out_dev + off, bytes, cudaMemcpyDeviceToHost, p.out));
   }
   if (good) good = ok(cudaEventRecord(p.out_end, p.out)) && ok(cudaStreamWaitEvent(s, p.out_end, 0));
   // Drain all three streams, after an error too, so that no copy still uses

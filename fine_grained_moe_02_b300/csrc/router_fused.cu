@@ -401,8 +401,8 @@ int run_fused(const RouteArgs& a, int head_dim, cudaStream_t stream) {
   fa.groups = G;
   fa.partial = a.partial;
   auto kern = router_fused_kernel<BNE>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRDynBytes) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  static std::atomic<uint64_t> smem_set{0};
+  if (!smem_attr_ready(kern, kRDynBytes, smem_set)) return MOE_ERR_CUDA;
   const int64_t items = m_tiles * G;
   const int grid = static_cast<int>(items < a.sm_count ? items : a.sm_count);
   kern<<<grid, kGemmThreads, kRDynBytes, stream>>>(tx, tl, th, fa);

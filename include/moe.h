@@ -344,10 +344,11 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
 /* moe_forward for a caller whose activations live in host memory: x_host
  * [T, d] in, out_host [T, d] out, weights on the device; returns after the
  * result is in out_host (the call synchronises `stream`).  The layer runs
- * over n = min(ceil(T / 8192), 8) token chunks of ceil(T / n) tokens: the
- * chunks' copies to the device run on one internal stream and the copies
- * back on another, overlapping the compute of the neighbouring chunks on
- * `stream`.  Each token's result has the same bits as moe_forward over the
+ * over n = min(ceil(T / 8192), 8) token chunks of ceil(T / n) tokens (for
+ * n >= 3 the first and last chunk are cut 1:3, the short piece at the end of
+ * the batch): the chunks' copies to the device run on one internal stream
+ * and the copies back on another, overlapping the compute of the
+ * neighbouring chunks on `stream`.  Each token's result has the same bits as moe_forward over the
  * whole batch.  The device status word at the start of ws collects the flags
  * of every chunk.  Host buffers should be page-locked: pageable memory still
  * gives correct results, but the copies then serialise with the compute.

@@ -136,3 +136,33 @@ def test_pipeline_wait_timeout_is_reported_and_the_context_survives():
     assert dev.status() == 0
     ref = O.forward_bits(inp, topk_idx=idx.cpu().numpy())
     G.check_out(G.host_f64(out), ref["out"])
+
+
+def test_forward_captured_in_a_cuda_graph_replays_with_new_inputs():
+    # group sizes stay on the device, so one captured moe_forward serves any
+    # routing: replaying it on new x gives the bits of a direct call
+    inp = G.small_inputs(T=3000, d=512, E=32, inter=256, seed=5)
+    dev = G.Dev(inp)
+    ref1 = dev.forward()  # first launches (and kernel attributes) outside the capture
+    g2 = torch.Generator(device="cpu").manual_seed(11)
+    x2 = (torch.randn(dev.x.shape, generator=g2) * 1.5).to(torch.bfloat16).cuda()
+    x_buf = dev.x.clone()
+    ref2 = torch.empty_like(ref1)
+    moe.moe_forward(dev.dims, x2, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, ref2, dev.ws)
+    torch.cuda.synchronize()
+    out = torch.full_like(ref1, float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        moe.moe_forward(dev.dims, x_buf, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, out, dev.ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    assert torch.equal(out.view(torch.int16), ref1.view(torch.int16))
+    x_buf.copy_(x2)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert dev.status() == 0
+    assert torch.equal(out.view(torch.int16), ref2.view(torch.int16))
+    assert not torch.equal(ref1.view(torch.int16), ref2.view(torch.int16))
