@@ -139,8 +139,10 @@ struct EpiSwiGLU {
         tmem_ld32(taddr + j * 128 + 64 + h * 32, u);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a0 = g[2 * i] / (1.0f + __expf(-g[2 * i])) * u[2 * i];
-          const float a1 = g[2 * i + 1] / (1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
+          // silu(g) = g / (1 + e^-g) with the fast division (~2 ulp of fp32, far
+          // below the bf16 rounding that follows); e^-g = inf for g < -88 gives 0
+          const float a0 = __fdividef(g[2 * i], 1.0f + __expf(-g[2 * i])) * u[2 * i];
+          const float a1 = __fdividef(g[2 * i + 1], 1.0f + __expf(-g[2 * i + 1])) * u[2 * i + 1];
           pk[j * 32 + h * 16 + i] = pack_bf16x2(a0, a1);
         }
       }
