@@ -39,6 +39,7 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
   // the B tensor map must deliver exactly this kernel's per-CTA B slice, or
   // the stage byte count and the shared-memory ring would disagree
   if (b_box_rows != BN / CL) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (shape.groups < 1 || shape.groups > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;  // shared tile table
   auto kern = gemm_tc_kernel<BN, Epi, CL>;
   // once per device: later calls (and stream captures) launch without it
   static std::atomic<uint64_t> smem_set{0};

@@ -31,6 +31,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "internal.h"
 #include "moe.h"
 #include "ptx.cuh"
 
@@ -39,7 +40,7 @@ namespace moe {
 constexpr int kBM = 128;          // tile rows (UMMA M)
 constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of bf16
 constexpr int kUK = 16;           // k per tcgen05.mma (kind::f16)
-constexpr int kMaxGroups = 256;
+constexpr int kMaxGroups = kMaxGemmGroups;  // tile prefix table in shared memory
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kOutChunkBytes = 32 * 128;          // 32 rows x 64 bf16
@@ -105,8 +106,19 @@ struct TileCoord {
   int row_end;   // end of the group's rows (exclusive)
 };
 
+// First A row of group g (g = groups: the end of the last group): the device
+// offsets, or the dense layouts (one group of M rows; batched: g * M).
+struct GroupRows {
+  const int* offsets;
+  int batched;
+  int M;
+  __device__ __forceinline__ int operator()(int g) const {
+    return offsets ? __ldg(offsets + g) : (batched ? g * M : (g == 0 ? 0 : M));
+  }
+};
+
 template <int BN>
-__device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, const int* s_tile, int groups,
+__device__ __forceinline__ TileCoord decode_tile(int tile, const GroupRows& rows, const int* s_tile, int groups,
                                                  int n_tiles, int cl = 1, int crank = 0) {
   // largest g with s_tile[g] <= tile
   int lo = 0, hi = groups - 1;
@@ -119,8 +131,8 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const int* s_row, con
   const int local = tile - s_tile[lo];
   c.m_blk = local / n_tiles;
   c.n_blk = local - c.m_blk * n_tiles;
-  c.row0 = s_row[lo] + (c.m_blk * cl + crank) * kBM;
-  c.row_end = s_row[lo + 1];
+  c.row0 = rows(lo) + (c.m_blk * cl + crank) * kBM;
+  c.row_end = rows(lo + 1);
   return c;
 }
 
@@ -145,9 +157,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_row[kMaxGroups + 1];
   __shared__ int s_tile[kMaxGroups + 1];
   __shared__ int s_total;
+  __shared__ int s_bad;
 
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
   const int warp = threadIdx.x >> 5;
@@ -159,38 +171,46 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   const int tile_step = CL == 2 ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   constexpr uint16_t kPair = 0x3;
 
-  // ---- group table: row offsets and tile prefix (all threads, then warp 0 scans)
+  // ---- group table: tile counts of the groups (all threads; group rows come
+  // from the offsets in global memory, and again when a tile is decoded),
+  // then their exclusive prefix (warp 0, each lane summing a contiguous run)
   // (batched dense mode: every group spans rows [0, M); decode_tile maps them)
-  for (int i = threadIdx.x; i <= groups; i += blockDim.x)
-    s_row[i] = shape.offsets ? __ldg(shape.offsets + i) : (shape.batched ? i * shape.M : (i == 0 ? 0 : shape.M));
-  if (threadIdx.x == 0) s_abort = 0;
+  const GroupRows rows{shape.offsets, shape.batched, shape.M};
+  const int row_limit = shape.batched ? groups * shape.M : shape.M;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+    const int a = rows(g), b = rows(g + 1);
+    int cnt = 0;
+    if (a < 0 || b < a || b > row_limit) s_bad = 1;
+    else cnt = ((b - a + CL * kBM - 1) / (CL * kBM)) * n_tiles;
+    s_tile[g] = cnt;
+  }
   __syncthreads();
   if (warp == 0) {
-    // per-group m-tile counts, validated; exclusive scan by one warp
-    bool bad = false;
-    int carry = 0;
-    for (int base = 0; base < groups; base += 32) {
-      const int g = base + lane;
-      int cnt = 0;
-      if (g < groups) {
-        const int a = s_row[g], b = s_row[g + 1];
-        if (a < 0 || b < a || b > (shape.batched ? groups * shape.M : shape.M)) bad = true;
-        else cnt = ((b - a + CL * kBM - 1) / (CL * kBM)) * n_tiles;
-      }
-      int incl = cnt;
+    const int per = (groups + 31) / 32;
+    const int g0 = min(lane * per, groups), g1 = min(g0 + per, groups);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += s_tile[g];
+    int incl = sum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (g < groups) s_tile[g] = carry + incl - cnt;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
     }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      s_tile[groups] = carry;
-      s_total = bad ? 0 : carry;
-      if (bad && blockIdx.x == 0) atomicOr(shape.status, MOE_DEV_BAD_OFFSETS);
+    int run = incl - sum;
+    for (int g = g0; g < g1; ++g) {
+      const int c = s_tile[g];
+      s_tile[g] = run;
+      run += c;
+    }
+    if (lane == 31) {
+      s_tile[groups] = incl;
+      s_total = s_bad ? 0 : incl;
+      if (s_bad && blockIdx.x == 0) atomicOr(shape.status, MOE_DEV_BAD_OFFSETS);
     }
   }
   if (threadIdx.x == 0) {
@@ -235,7 +255,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     uint32_t filled = 0, last_par = 0;
     bool ok = true;
     for (int tile = first_tile; tile < total && ok; tile += tile_step) {
-      const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles);
+      const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
       const int b_row = c.group * shape.N + c.n_blk * BN;
       int src[4];
 #pragma unroll
@@ -293,7 +313,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
       bool ok = true;
       for (int tile = first_tile; tile < total && ok && !shape.selftest_stall; tile += tile_step) {
-        const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles, CL, crank);
+        const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles, CL, crank);
         const int b_row = c.group * (shape.b_group_rows ? shape.b_group_rows : shape.N) + c.n_blk * BN;
         const int a_row = shape.batched ? c.row0 - c.group * shape.M : c.row0;
         const int a_col = shape.batched ? c.group * shape.a_col_stride : 0;
@@ -398,7 +418,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         break;
       }
       ptx::tc_fence_after();
-      const TileCoord c = decode_tile<BN>(tile, s_row, s_tile, groups, n_tiles, CL, crank);
+      const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles, CL, crank);
       ctx.tempty = ptx::smem_u32(&tempty_bar[acc]);
       ctx.released = false;
       // an epilogue may hand the accumulator back itself (release_accumulator)

@@ -2,8 +2,10 @@
 // into head slices; head j routes its own slice over its own E experts (router
 // GEMM + fused top-k), sorts its tokens, runs its head-local SwiGLU experts
 // (head_dim -> inter -> head_dim, grouped tcgen05 GEMMs) and combines into its
-// head_dim columns of out.  The heads run one after another on the caller's
-// stream and reuse one set of per-head buffers in the workspace.
+// head_dim columns of out.  All heads go through each stage together: one
+// batched router GEMM, one sort/gather over (head, token), one grouped GEMM
+// per expert layer over all n_heads * E head-local experts (head by head only
+// when they exceed the engine's group table), one combine.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -28,19 +30,21 @@ int check_hl(const moe_dims* d) {
   if (d->head_dim % 64 != 0 || d->inter % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d->E > kMaxExperts || d->top_k > kMaxTopK || d->top_k > d->E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d->T * d->top_k >= (static_cast<int64_t>(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (static_cast<int64_t>(d->E) * 2 * d->inter >= (static_cast<int64_t>(1) << 31) ||
-      static_cast<int64_t>(d->n_heads) * d->E * d->head_dim >= (static_cast<int64_t>(1) << 31))
+  if (static_cast<int64_t>(d->n_heads) * d->E * 2 * d->inter >= (static_cast<int64_t>(1) << 31) ||
+      static_cast<int64_t>(d->n_heads) * d->E * d->head_dim >= (static_cast<int64_t>(1) << 31) ||
+      static_cast<int64_t>(d->n_heads) * d->T * d->top_k >= (static_cast<int64_t>(1) << 31))
     return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
 struct HlLayout {
-  size_t disp, idx, gate, offsets, row_of, src, xperm, act, end;
+  size_t disp, idx, gate, offsets, goff, row_of, src, xperm, act, end;
 };
 
 // Per-head arrays side by side: idx/gate/row_of/src [H, T, k], offsets [H, E+1],
-// x_perm (then y_perm) [H, T*k, head_dim], dispatch counters [2][H][nblk][E];
-// act [T*k, inter] is reused head by head.
+// x_perm (then y_perm) [H, T*k, head_dim], act [H, T*k, inter], dispatch
+// counters [2][H][nblk][E]; goff [H*E + 1]: the group offsets of all heads'
+// experts over the concatenated rows (head h's rows start at h*T*k).
 HlLayout hl_layout(const moe_dims* d) {
   HlLayout l;
   const size_t H = d->n_heads;
@@ -49,12 +53,24 @@ HlLayout hl_layout(const moe_dims* d) {
   l.idx = align_up(l.disp + H * dispatch_scratch_bytes(d->T, d->E), kAlign);
   l.gate = align_up(l.idx + H * Tk * 4, kAlign);
   l.offsets = align_up(l.gate + H * Tk * 4, kAlign);
-  l.row_of = align_up(l.offsets + H * (static_cast<size_t>(d->E) + 1) * 4, kAlign);
+  l.goff = align_up(l.offsets + H * (static_cast<size_t>(d->E) + 1) * 4, kAlign);
+  l.row_of = align_up(l.goff + (H * d->E + 1) * 4, kAlign);
   l.src = align_up(l.row_of + H * Tk * 4, kAlign);
   l.xperm = align_up(l.src + H * Tk * 4, kAlign);
   l.act = align_up(l.xperm + H * Tk * d->head_dim * 2, kAlign);
-  l.end = align_up(l.act + Tk * d->inter * 2, kAlign);
+  l.end = align_up(l.act + H * Tk * d->inter * 2, kAlign);
   return l;
+}
+
+// goff[h*E + e] = h*Tk + offsets[h][e], goff[H*E] = H*Tk.
+__global__ void concat_offsets_kernel(const int32_t* __restrict__ offsets, int H, int E, int64_t Tk,
+                                      int32_t* __restrict__ goff) {
+  const int64_t n = static_cast<int64_t>(H) * E;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i <= n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t h = i / E, e = i - h * E;
+    goff[i] = static_cast<int32_t>(i == n ? H * Tk : h * Tk + offsets[h * (E + 1) + e]);
+  }
 }
 
 template <class T>
@@ -136,23 +152,44 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
   da.sm_count = sms;
   if ((rc = launch_dispatch(da, s)) != MOE_OK) return rc;
 
-  // 3. each head's grouped expert GEMMs (y_perm overwrites the head's x_perm)
-  for (int j = 0; j < H; ++j) {
-    FfnArgs fa{};
-    fa.offsets = da.offsets + static_cast<int64_t>(j) * (E + 1);
-    fa.rows = Tk;
-    fa.d = Dh;
-    fa.I = I;
-    fa.E = E;
-    fa.status = status;
-    fa.sm_count = sms;
-    fa.x_perm = da.x_perm + static_cast<int64_t>(j) * Tk * Dh;
-    fa.w13 = w13 + static_cast<int64_t>(j) * E * 2 * I * Dh;
-    fa.act = at<uint16_t>(ws, l.act);
+  // 3. the grouped expert GEMMs over all heads' experts at once (group h*E + e
+  //    = expert e of head h; y_perm overwrites x_perm); head by head when the
+  //    n_heads * E groups exceed the engine's table
+  FfnArgs fa{};
+  fa.d = Dh;
+  fa.I = I;
+  fa.status = status;
+  fa.sm_count = sms;
+  uint16_t* act = at<uint16_t>(ws, l.act);
+  if (static_cast<int64_t>(H) * E <= kMaxGemmGroups) {
+    int32_t* goff = at<int32_t>(ws, l.goff);
+    const int64_t n = static_cast<int64_t>(H) * E + 1;
+    const int blocks = static_cast<int>((n + 255) / 256 < sms ? (n + 255) / 256 : sms);
+    concat_offsets_kernel<<<blocks, 256, 0, s>>>(da.offsets, H, E, Tk, goff);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    fa.offsets = goff;
+    fa.rows = static_cast<int64_t>(H) * Tk;
+    fa.E = H * E;
+    fa.x_perm = da.x_perm;
+    fa.w13 = w13;
+    fa.act = act;
     if ((rc = launch_gemm1(fa, s)) != MOE_OK) return rc;
-    fa.w_down = w_down + static_cast<int64_t>(j) * E * Dh * I;
-    fa.y_perm = da.x_perm + static_cast<int64_t>(j) * Tk * Dh;
+    fa.w_down = w_down;
+    fa.y_perm = da.x_perm;
     if ((rc = launch_gemm2(fa, s)) != MOE_OK) return rc;
+  } else {
+    for (int j = 0; j < H; ++j) {
+      fa.offsets = da.offsets + static_cast<int64_t>(j) * (E + 1);
+      fa.rows = Tk;
+      fa.E = E;
+      fa.x_perm = da.x_perm + static_cast<int64_t>(j) * Tk * Dh;
+      fa.w13 = w13 + static_cast<int64_t>(j) * E * 2 * I * Dh;
+      fa.act = act + static_cast<int64_t>(j) * Tk * I;
+      if ((rc = launch_gemm1(fa, s)) != MOE_OK) return rc;
+      fa.w_down = w_down + static_cast<int64_t>(j) * E * Dh * I;
+      fa.y_perm = da.x_perm + static_cast<int64_t>(j) * Tk * Dh;
+      if ((rc = launch_gemm2(fa, s)) != MOE_OK) return rc;
+    }
   }
 
   // 4. every head's combine into its columns of out, one launch

@@ -11,6 +11,7 @@ namespace moe {
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
+constexpr int kMaxGemmGroups = 3072;  // row groups of one grouped-GEMM launch
 
 // Raises a kernel's dynamic shared-memory limit on the current device the
 // first time it is launched there; `done` (one per kernel) holds one bit per

@@ -55,6 +55,8 @@ def _check(inp, out, idx, logits, tokens=None):
     dict(T=300, d=128, n_heads=2, head_dim=64, E=8, inter=64, top_k=2),
     dict(T=1000, d=512, n_heads=4, head_dim=128, E=32, inter=128, top_k=6),
     dict(T=129, d=768, n_heads=3, head_dim=256, E=256, inter=64, top_k=8),
+    # 16 x 256 head-local experts exceed one grouped-GEMM launch: head by head
+    dict(T=200, d=1024, n_heads=16, head_dim=64, E=256, inter=64, top_k=2),
 ])
 def test_headlocal_matches_oracle(kw):
     inp = mi.make_inputs(mi.custom_config("hl", head_local=True, **kw))
