@@ -286,6 +286,26 @@ __device__ __forceinline__ void write_topk(const TopKParams& p, int row, const f
   }
 }
 
+// Inserts (s, e) into the descending list bv/bi (kMaxTopK slots) when s beats
+// its last entry.  The list is sorted, so slot q keeps its entry when it is
+// >= s, takes s when slot q-1 is >= s (or q = 0), and otherwise takes slot
+// q-1's entry: every slot is decided from two comparisons, no chain of
+// swaps.  Entries equal to s stay ahead of it (e grows along the row, so ties
+// go to the lower expert index).
+__device__ __forceinline__ void topk_insert(float (&bv)[kMaxTopK], int (&bi)[kMaxTopK], float s, int e) {
+  bool ge[kMaxTopK];
+#pragma unroll
+  for (int q = 0; q < kMaxTopK; ++q) ge[q] = bv[q] >= s;
+#pragma unroll
+  for (int q = kMaxTopK - 1; q >= 0; --q) {
+    const bool put = (q == 0) || ge[q - 1];
+    const float shifted_v = q > 0 ? bv[q - 1] : s;
+    const int shifted_i = q > 0 ? bi[q - 1] : e;
+    bv[q] = ge[q] ? bv[q] : (put ? s : shifted_v);
+    bi[q] = ge[q] ? bi[q] : (put ? e : shifted_i);
+  }
+}
+
 template <int BN>
 __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, int row, bool valid) {
   float bv[kMaxTopK];
@@ -296,31 +316,21 @@ __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, in
   expert_range(p, row, valid, &e_lo, &e_hi);
   float* lrow = (p.logits != nullptr && valid) ? p.logits + static_cast<int64_t>(row) * p.E : nullptr;
 #pragma unroll 1
-  for (int col = 0; col < BN; col += 16) {
-    uint32_t u[16];
+  for (int col = 0; col < BN; col += 32) {
+    uint32_t u[32];
     __syncwarp();
-    ptx::tmem_ld16(taddr + col, u);
+    ptx::tmem_ld16(taddr + col, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+    if (col + 16 < BN) ptx::tmem_ld16(taddr + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
     ptx::tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < 32; ++j) {
       const int e = col + j;
-      if (e < p.E) {
-        float s = __uint_as_float(u[j]);
-        if (p.bias != nullptr) s += __ldg(p.bias + e);
-        if (lrow != nullptr) lrow[e] = s;
-        if (e >= e_lo && e < e_hi && s > bv[kMaxTopK - 1]) {
-          float cv = s;
-          int ci = e;
-#pragma unroll
-          for (int q = 0; q < kMaxTopK; ++q) {
-            const bool gt = cv > bv[q];
-            const float tv = gt ? bv[q] : cv;
-            const int ti = gt ? bi[q] : ci;
-            bv[q] = gt ? cv : bv[q];
-            bi[q] = gt ? ci : bi[q];
-            cv = tv;
-            ci = ti;
-          }
+      if (j < 16 || col + 16 < BN) {
+        if (e < p.E) {
+          float s = __uint_as_float(u[j]);
+          if (p.bias != nullptr) s += __ldg(p.bias + e);
+          if (lrow != nullptr) lrow[e] = s;
+          if (e >= e_lo && e < e_hi && s > bv[kMaxTopK - 1]) topk_insert(bv, bi, s, e);
         }
       }
     }

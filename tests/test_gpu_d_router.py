@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 import torch
 
+import fine_grained_moe_02_b300 as moe
 import moe_inputs as mi
 from tests import gpu_util as G
 
@@ -68,3 +69,47 @@ def test_fused_router_full_clip_sampled():
     tok = mi.sample_tokens(cfg.T, 512, seed=13)
     G.check_routing(G.oracle_logits(inp, tok), idx.cpu().numpy()[tok], gate.cpu().numpy()[tok], cfg.top_k,
                     logits[torch.from_numpy(tok).cuda()].cpu().numpy())
+
+
+@pytest.mark.parametrize("path", ["two_stage", "fused", "folded"])
+def test_exact_ties_go_to_the_lower_index(path):
+    # experts e, e+8, e+16, e+24 share a W_head row and a bias, so they score
+    # exactly alike on every token: the top-6 boundary falls inside a tie
+    # group, where only the lower expert indices may be taken, in index order
+    inp = G.small_inputs(T=400, d=512, E=32, inter=64, seed=9)
+    cfg = inp["cfg"]
+    ng, E = 8, 32
+    inp["w_head"] = np.ascontiguousarray(inp["w_head"][np.arange(E) % ng])
+    gb = np.random.default_rng(4).normal(0.0, 2.0, ng).astype(np.float32)
+    inp["bias"] = np.ascontiguousarray(gb[np.arange(E) % ng])
+    dev = G.Dev(inp)
+    if path == "two_stage":
+        idx, gate, logits = dev.route()
+    elif path == "fused":
+        idx, gate, logits = dev.route_fused()
+    else:
+        w = torch.empty((E, 2 * cfg.d), dtype=torch.bfloat16, device="cuda")
+        moe.moe_prepare_router(dev.dims, dev.w_lat, dev.w_head, w)
+        idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+        gate = torch.empty((cfg.T, cfg.top_k), dtype=torch.float32, device="cuda")
+        logits = torch.empty((cfg.T, E), dtype=torch.float32, device="cuda")
+        moe.moe_route_folded(dev.dims, dev.x, w, dev.bias, idx, gate, logits, dev.ws)
+    assert dev.status() == 0
+    lg = logits.cpu().numpy()
+    members = [np.arange(g, E, ng) for g in range(ng)]
+    for g in range(ng):
+        assert np.all(lg[:, members[g]] == lg[:, [g]])  # tied experts: bit-identical logits
+    gv = G.oracle_logits(inp)[:, :ng]  # one value per tie group
+    order = np.argsort(-gv, axis=1, kind="stable")
+    want = np.array([np.concatenate([members[g] for g in row])[:cfg.top_k] for row in order])
+    clear = np.min(np.diff(np.sort(gv, axis=1), axis=1), axis=1) > 1e-3  # groups apart by > 1e-3
+    assert clear.sum() > 0.9 * cfg.T
+    np.testing.assert_array_equal(idx.cpu().numpy()[clear], want[clear])
+    g = gate.cpu().numpy()[clear]
+    same = np.take_along_axis(lg[clear], idx.cpu().numpy()[clear], axis=1)
+    # equal logits get equal gates
+    for t in range(g.shape[0]):
+        for a in range(cfg.top_k):
+            for b in range(a + 1, cfg.top_k):
+                if same[t, a] == same[t, b]:
+                    assert g[t, a] == g[t, b]
