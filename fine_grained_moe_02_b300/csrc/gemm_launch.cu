@@ -32,7 +32,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-template <int BN, class Epi, int CL = 1>
+template <int BN, class Epi, int CL = 1, int GW = 0>
 int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmShape& shape,
              const typename Epi::Params& ep, int grid, cudaStream_t stream, int b_box_rows) {
   using S = GemmSmem<BN>;
@@ -40,13 +40,15 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
   // the stage byte count and the shared-memory ring would disagree
   if (b_box_rows != BN / CL) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (shape.groups < 1 || shape.groups > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;  // shared tile table
-  auto kern = gemm_tc_kernel<BN, Epi, CL>;
+  if ((GW > 0) != (shape.a_gather != nullptr)) return MOE_ERR_UNSUPPORTED_SHAPE;  // gathered A needs gather warps
+  auto kern = gemm_tc_kernel<BN, Epi, CL, GW>;
+  constexpr int kThreads = kGemmThreads + 32 * GW;
   // once per device: later calls (and stream captures) launch without it
   static std::atomic<uint64_t> smem_set{0};
   if (!smem_attr_ready(kern, S::kDynBytes, smem_set)) return MOE_ERR_CUDA;
   if (grid < 1) grid = 1;
   if constexpr (CL == 1) {
-    kern<<<grid, kGemmThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);
+    kern<<<grid, kThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   } else {
     // Persistent grid of CTA pairs: never more pairs than can be resident at
@@ -221,17 +223,19 @@ int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
 // x[src_token[r]], fetched four rows at a time by TMA tile::gather4, so the
 // permuted copy x_perm never exists.
 int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream) {
-  CUtensorMap ta, tb, td;
+  // A rows come from x through src_token (cp.async gather warps); tmap_a is unused
+  CUtensorMap tb, td;
   const int rows = static_cast<int>(a.rows);
   const int n = 2 * a.I;
   const int bn = (n % 256 == 0) ? 256 : 128;
-  if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, 1)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&td, a.act, a.I, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status, a.src_token};
+  sh.a_src = a.x;
+  sh.a_ld = a.d;
   EpiSwiGLU::Params ep{a.act, a.I};
-  return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn)
-                     : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn);
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU, 1, 2>(tb, tb, td, sh, ep, a.sm_count, stream, bn)
+                     : run_gemm<128, EpiSwiGLU, 1, 2>(tb, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
 // Expert GEMM-2 over ragged groups: y_perm = act Wd^T.

@@ -53,9 +53,9 @@ struct GemmShape {
   const int* offsets;  // device [groups + 1], or nullptr: one group of rows [0, M)
   int M;            // rows when offsets == nullptr; row capacity of A otherwise
   int* status;      // device status word
-  // Row gather for A: if non-null, logical A row r is row a_gather[r] of the
-  // tensor behind tmap_a (a [*, K] matrix whose map has a 64 x 1 box), loaded
-  // with TMA tile::gather4 by the whole producer warp.
+  // Row gather for A (kernels with gather warps, GW > 0): logical A row r is
+  // row a_gather[r] of a_src, a row-major [*, K] bf16 matrix with a_ld
+  // elements per row; tmap_a is not used.
   const int* a_gather;
   // A's k coordinate is k % K_A (0 means K): one A tile serves a K = c*K_A
   // sweep (the folded router reads x twice, against W_eff's hi and lo halves).
@@ -71,7 +71,16 @@ struct GemmShape {
   int batched;
   int a_col_stride;
   int b_group_rows;
+  const uint16_t* a_src;
+  int64_t a_ld;
 };
+
+// Gather warps: the A operand's rows are fetched by 32*GW threads with 16-byte
+// cp.async copies, 8 lanes per 128-byte row slice (4 whole rows per warp
+// instruction); a thread signals a stage kGatherLag k-slices after issuing it,
+// once its own copies have landed (cp.async.wait_group) and a proxy fence has
+// ordered them before the tensor core's reads.
+constexpr int kGatherLag = 2;
 
 template <int BN>
 struct GemmSmem {
@@ -141,8 +150,8 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GroupRows& rows
 //   template <int BN> static __device__ void run(const Params&, const TileCoord&, uint32_t taddr,
 //                                                 int row_in_tile, EpiCtx&);
 // taddr addresses this thread's lane (= tile row) at the accumulator's column 0.
-template <int BN, class Epi, int CL = 1>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, class Epi, int CL = 1, int GW = 0>
+__global__ void __launch_bounds__(kGemmThreads + 32 * GW, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d, GemmShape shape, typename Epi::Params ep) {
   using S = GemmSmem<BN>;
@@ -162,6 +171,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ int s_bad;
 
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
+  static_assert(GW == 0 || (CL == 1 && kBM % (4 * GW) == 0), "gather warps: single CTAs");
+  static_assert(kGatherLag < STAGES, "a gather thread must be able to issue past the stage it signals");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = shape.N / BN;
@@ -215,7 +226,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1 + 32 * GW);  // the B (+A) loader, every gather thread
       ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), CL);  // every CTA's MMA frees the stage in all CTAs
     }
     for (int b = 0; b < 2; ++b) {
@@ -245,23 +256,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   const int num_kb = shape.K / kBK;
   const uint64_t wait_ns = shape.wait_limit_ns ? shape.wait_limit_ns : kWaitLimitNs;
 
-  if (warp == 0 && shape.a_gather != nullptr) {
-    // ------------------------------------------------------ producer (gather)
-    // Lane l owns A rows 4l .. 4l+3 of every tile: it looks up their source
-    // rows once per tile and issues one gather4 per k-block; lane 0 also
-    // waits for free slots, posts the expected bytes and loads B.
+  if (GW > 0 && warp >= kGemmThreads / 32) {
+    // -------------------------------------------------------- A gather warps
+    const int gt = static_cast<int>(threadIdx.x) - kGemmThreads;  // 0 .. 32*GW - 1
+    constexpr int kRowStep = 4 * (GW > 0 ? GW : 1);               // rows per instruction of all gather warps
+    constexpr int kRowsPer = kBM / kRowStep;                      // rows per thread per k-slice
+    const int chunk = gt & 7;                                     // this lane's 16-byte chunk of a row slice
+    const int r_first = gt >> 3;                                  // rows r_first + j * kRowStep
+    const uint32_t dst_off = static_cast<uint32_t>(r_first) * 128u +
+                             ((static_cast<uint32_t>(chunk) ^ (static_cast<uint32_t>(r_first) & 7u)) << 4);
+    const uint64_t pol = ptx::policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t filled = 0, last_par = 0;
+    int64_t issued = 0;
     bool ok = true;
     for (int tile = first_tile; tile < total && ok; tile += tile_step) {
       const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
-      const int b_row = c.group * shape.N + c.n_blk * BN;
-      int src[4];
+      const uint16_t* src[kRowsPer];
+      uint32_t valid = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = c.row0 + 4 * lane + j;
-        src[j] = row < c.row_end ? __ldg(shape.a_gather + row) : 0;
+      for (int j = 0; j < kRowsPer; ++j) {
+        const int row = c.row0 + r_first + j * kRowStep;
+        const bool v = row < c.row_end;
+        const int tok = v ? __ldg(shape.a_gather + row) : 0;
+        src[j] = shape.a_src + static_cast<int64_t>(tok) * shape.a_ld + chunk * 8;
+        valid |= (v ? 1u : 0u) << j;
       }
       for (int kb = 0; kb < num_kb; ++kb) {
         bool got = true;
@@ -270,34 +289,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
           ok = false;
           break;
         }
-        const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
-        const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
-        const int k = kb * kBK;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(fb, S::kStageBytes);
-        __syncwarp();
-        ptx::tma_gather4(sa + static_cast<uint32_t>(lane) * 512u, &tmap_a, k, src[0], src[1], src[2], src[3], fb);
-        if (lane == 0) {
-          ptx::tma_load_2d(sa + S::kABytes, &tmap_b, k % shape.K_B, b_row, fb, ptx::policy_evict_last());
-          filled |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes) + dst_off;
+#pragma unroll
+        for (int j = 0; j < kRowsPer; ++j)  // row r_first + j*kRowStep keeps the swizzle of r_first (kRowStep % 8 == 0)
+          ptx::cp_async_16(sa + static_cast<uint32_t>(j * kRowStep) * 128u, src[j] + kb * kBK,
+                           ((valid >> j) & 1u) ? 16u : 0u, pol);
+        ptx::cp_async_commit();
+        if (issued >= kGatherLag) {
+          ptx::cp_async_wait<kGatherLag>();
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(ptx::smem_u32(&full_bar[(issued - kGatherLag) % STAGES]));
         }
+        ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     }
-    if (lane == 0) {
-      if (!ok) {
-        atomicOr(shape.status, MOE_DEV_TIMEOUT);
-        s_abort = 1;
-      }
-      for (int s = 0; s < STAGES; ++s) {
-        if (filled & (1u << s)) {
-          const volatile int never = 0;
-          if (!ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, wait_ns))
-            atomicOr(shape.status, MOE_DEV_TIMEOUT);
-        }
-      }
+    if (!ok && lane == 0) {
+      atomicOr(shape.status, MOE_DEV_TIMEOUT);
+      s_abort = 1;
     }
-    __syncwarp();
+    // drain: this thread's copies land, and its last stages are signaled
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    for (int64_t i = issued > kGatherLag ? issued - kGatherLag : 0; i < issued; ++i)
+      ptx::mbar_arrive(ptx::smem_u32(&full_bar[i % STAGES]));
   } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -323,11 +338,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             break;
           }
           const uint32_t fb = ptx::smem_u32(&full_bar[stage]);
-          ptx::mbar_arrive_expect_tx(fb, S::kStageBytes);
+          ptx::mbar_arrive_expect_tx(fb, GW > 0 ? S::kBBytes : S::kStageBytes);  // gathered A arrives by cp.async
           const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
           const uint32_t sb = sa + S::kABytes;
           const int k = kb * kBK;
-          ptx::tma_load_2d(sa, &tmap_a, a_col + (shape.K_A > 0 ? k % shape.K_A : k), a_row, fb, pol_a);
+          if (GW == 0)
+            ptx::tma_load_2d(sa, &tmap_a, a_col + (shape.K_A > 0 ? k % shape.K_A : k), a_row, fb, pol_a);
           if constexpr (CL == 2) {  // this CTA's half of B, into both CTAs
             constexpr int kHalf = BN / 2;
             ptx::tma_load_2d_multicast(sb + crank * kHalf * 128, &tmap_b, k % shape.K_B, b_row + crank * kHalf, fb,

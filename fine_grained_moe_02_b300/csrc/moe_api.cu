@@ -192,9 +192,9 @@ int forward_impl(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat,
   moe_bf16* xperm = at<moe_bf16>(ws, f.xperm);
   moe_bf16* act = at<moe_bf16>(ws, f.act);
   // y_perm reuses x_perm's memory: x_perm is dead once expert GEMM-1 has run.
-  // (moe_expert_gemm1_gather would skip x_perm entirely, but on B300 its
-  // four-row TMA gathers are issue-bound and GEMM-1 runs ~3x slower, more
-  // than the ~1.2 ms the separate gather costs on the clip workload.)
+  // (moe_expert_gemm1_gather skips x_perm entirely, its A rows fetched by
+  // cp.async gather warps, but on the clip workload it runs 9.8-9.9 ms
+  // against 8.0-8.3 ms for GEMM-1 on x_perm plus ~1.05 ms for the gather.)
   moe_bf16* yperm = xperm;
   if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;

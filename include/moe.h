@@ -241,12 +241,13 @@ int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t
                      moe_bf16* act, void* ws, size_t ws_bytes, void* stream);
 /* moe_expert_gemm1 with the sorting gather fused into the operand loads:
  * row r of the A operand is x[src_token[r]] (x [T, d], src_token from
- * moe_dispatch / moe_dispatch_indices), fetched by the tensor-memory
- * accelerator four rows at a time, so x_perm is never materialised (saves
- * T*top_k*d*2 bytes of memory and the gather's HBM round trip).  The result
- * equals moe_expert_gemm1 on the gathered x_perm bit for bit.  On B300 the
- * per-row gathers make this ~3x slower than moe_dispatch + moe_expert_gemm1,
- * so moe_forward does not use it. */
+ * moe_dispatch / moe_dispatch_indices), fetched with 16-byte asynchronous
+ * copies by two extra warps of the GEMM kernel, so x_perm is never
+ * materialised (saves T*top_k*d*2 bytes of memory and the gather's HBM round
+ * trip).  The result equals moe_expert_gemm1 on the gathered x_perm bit for
+ * bit.  On B300 it is ~1 ms slower on the clip workload than the separate
+ * gather plus moe_expert_gemm1 (the copies are handed to the tensor core
+ * stage by stage, two k-slices behind), so moe_forward does not use it. */
 int moe_expert_gemm1_gather(const moe_dims* dims, const moe_bf16* x, const int32_t* src_token,
                             const int32_t* offsets, const moe_bf16* w13, moe_bf16* act, void* ws, size_t ws_bytes,
                             void* stream);
