@@ -40,6 +40,11 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
   // the stage byte count and the shared-memory ring would disagree
   if (b_box_rows != BN / CL) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (shape.groups < 1 || shape.groups > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;  // shared tile table
+  {  // the kernel counts tiles in 32-bit ints: at most (rows / tile rows + groups) m-tiles per n-tile
+    const int64_t rows_all = shape.batched ? static_cast<int64_t>(shape.groups) * shape.M : shape.M;
+    const int64_t m_tiles = rows_all / (CL * kBM) + shape.groups;
+    if (shape.N % BN != 0 || m_tiles * (shape.N / BN) >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
   if ((GW > 0) != (shape.a_gather != nullptr)) return MOE_ERR_UNSUPPORTED_SHAPE;  // gathered A needs gather warps
   auto kern = gemm_tc_kernel<BN, Epi, CL, GW>;
   constexpr int kThreads = kGemmThreads + 32 * GW;
