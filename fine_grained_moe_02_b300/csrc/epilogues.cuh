@@ -84,6 +84,7 @@ __device__ __forceinline__ int warp_valid_rows(const TileCoord& c, const EpiCtx&
 // accumulator released, so the MMAs of a later tile do not wait for the
 // bulk stores of this one.
 struct EpiStoreBf16 {
+  static constexpr int kWarps = 4;
   struct Params {
     uint16_t* out;
     int64_t ld;
@@ -117,6 +118,7 @@ struct EpiStoreBf16 {
 // act[row, n_blk*BN/2 + 64*j + i] = bf16(silu(g) * u).  All of the row's
 // activations are formed in registers before the accumulator is released.
 struct EpiSwiGLU {
+  static constexpr int kWarps = 4;
   struct Params {
     uint16_t* act;
     int64_t ld;
@@ -160,6 +162,7 @@ struct EpiSwiGLU {
 // Router stage 1: latent h (fp32 accumulator) -> bf16 hi + lo pair.
 // hl[row, col] = hi, hl[row, L + col] = lo, with hi = bf16(h), lo = bf16(h - hi).
 struct EpiHiLo {
+  static constexpr int kWarps = 4;
   struct Params {
     uint16_t* hl;
     int64_t ld;  // 2L
@@ -306,6 +309,33 @@ __device__ __forceinline__ void topk_insert(float (&bv)[kMaxTopK], int (&bi)[kMa
   }
 }
 
+// Scans the row's columns [c0, c1) (multiples of 16) of the score
+// accumulator: bias, optional logits output, and the running top list for
+// experts in [e_lo, e_hi).
+__device__ __forceinline__ void topk_scan(const TopKParams& p, uint32_t taddr, int c0, int c1, int e_lo, int e_hi,
+                                          float* lrow, float (&bv)[kMaxTopK], int (&bi)[kMaxTopK]) {
+#pragma unroll 1
+  for (int col = c0; col < c1; col += 32) {
+    uint32_t u[32];
+    const bool two = col + 16 < c1;
+    __syncwarp();
+    ptx::tmem_ld16(taddr + col, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+    if (two) ptx::tmem_ld16(taddr + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = col + j;
+      if ((j < 16 || two) && e < p.E) {
+        float s = __uint_as_float(u[j]);
+        if (p.bias != nullptr) s += __ldg(p.bias + e);
+        if (lrow != nullptr) lrow[e] = s;
+        if (e >= e_lo && e < e_hi && s > bv[kMaxTopK - 1]) topk_insert(bv, bi, s, e);
+      }
+    }
+  }
+}
+
+// The whole row by one thread: scan all BN columns, then write the top k.
 template <int BN>
 __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, int row, bool valid) {
   float bv[kMaxTopK];
@@ -315,50 +345,89 @@ __device__ __forceinline__ void topk_row(const TopKParams& p, uint32_t taddr, in
   int e_lo, e_hi;
   expert_range(p, row, valid, &e_lo, &e_hi);
   float* lrow = (p.logits != nullptr && valid) ? p.logits + static_cast<int64_t>(row) * p.E : nullptr;
-#pragma unroll 1
-  for (int col = 0; col < BN; col += 32) {
-    uint32_t u[32];
-    __syncwarp();
-    ptx::tmem_ld16(taddr + col, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
-    if (col + 16 < BN) ptx::tmem_ld16(taddr + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
-    ptx::tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = col + j;
-      if (j < 16 || col + 16 < BN) {
-        if (e < p.E) {
-          float s = __uint_as_float(u[j]);
-          if (p.bias != nullptr) s += __ldg(p.bias + e);
-          if (lrow != nullptr) lrow[e] = s;
-          if (e >= e_lo && e < e_hi && s > bv[kMaxTopK - 1]) topk_insert(bv, bi, s, e);
-        }
-      }
-    }
-  }
+  topk_scan(p, taddr, 0, BN, e_lo, e_hi, lrow, bv, bi);
   if (!valid) return;
   write_topk(p, row, bv, bi);
 }
 
 // Router stage 2: summed head scores (fp32 accumulator, all E experts in one
-// tile) -> top-k epilogue.
+// tile) -> top-k epilogue.  One TMEM lane is one token.  Eight epilogue
+// warps: the two warps of a lane quadrant scan one half of the experts each;
+// the upper half's warp hands its list (through the staging area) to the
+// lower half's warp, which merges it in and writes the result.  Every
+// candidate of the upper half has a higher expert index than the lower
+// half's, so inserting them after it keeps ties with the lower index.
 struct EpiTopK {
   using Params = TopKParams;
+  static constexpr int kWarps = 8;
   template <int BN>
-  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
-                                             EpiCtx&) {
-    const int row = c.row0 + r;
-    if (p.T > 0) {  // batched: group c.group owns its own outputs
-      TopKParams q = p;
+  static __device__ __forceinline__ void run(const Params& p0, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx& ctx) {
+    const int row0 = c.row0 + r;
+    const bool valid = row0 < c.row_end;
+    TopKParams p = p0;
+    int row = row0;
+    if (p0.T > 0) {  // batched: group c.group owns its own outputs
       const int64_t g = c.group;
-      const int ko = p.k_out > 0 ? p.k_out : p.k;
-      q.idx = p.idx + g * p.T * ko;
-      q.gate = p.gate + g * p.T * ko;
-      if (p.logits != nullptr) q.logits = p.logits + g * p.T * p.E;
-      if (p.bias != nullptr) q.bias = p.bias + g * p.E;
-      topk_row<BN>(q, taddr, row - static_cast<int>(g) * p.T, row < c.row_end);
-      return;
+      const int ko = p0.k_out > 0 ? p0.k_out : p0.k;
+      p.idx = p0.idx + g * p0.T * ko;
+      p.gate = p0.gate + g * p0.T * ko;
+      if (p0.logits != nullptr) p.logits = p0.logits + g * p0.T * p0.E;
+      if (p0.bias != nullptr) p.bias = p0.bias + g * p0.E;
+      row = row0 - static_cast<int>(g) * p0.T;
     }
-    topk_row<BN>(p, taddr, row, row < c.row_end);
+    float bv[kMaxTopK];
+    int bi[kMaxTopK];
+#pragma unroll
+    for (int i = 0; i < kMaxTopK; ++i) { bv[i] = -INFINITY; bi[i] = -1; }
+    int e_lo, e_hi;
+    expert_range(p, row, valid, &e_lo, &e_hi);
+    float* lrow = (p.logits != nullptr && valid) ? p.logits + static_cast<int64_t>(row) * p.E : nullptr;
+    if constexpr (BN < 32) {  // one warp per quadrant is enough
+      if (ctx.part == 1) return;
+      topk_scan(p, taddr, 0, BN, e_lo, e_hi, lrow, bv, bi);
+    } else {
+      constexpr int kHalf = BN / 2;
+      const uint32_t vbuf = ctx.scratch, ibuf = ctx.scratch + kMaxTopK * kBM * 4;  // [slot][tile row]
+      const uint32_t parity = ctx.hand_uses & 1u;
+      ++ctx.hand_uses;
+      if (ctx.part == 1) {
+        topk_scan(p, taddr, kHalf, BN, e_lo, e_hi, lrow, bv, bi);
+        if (!ptx::mbar_wait(ctx.hand_free, parity ^ 1u, ctx.abort, ctx.wait_ns)) {
+          ctx.failed = true;
+          return;
+        }
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q) {
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(vbuf + static_cast<uint32_t>((q * kBM + r) * 4)), "f"(bv[q])
+                       : "memory");
+          asm volatile("st.shared.s32 [%0], %1;" ::"r"(ibuf + static_cast<uint32_t>((q * kBM + r) * 4)), "r"(bi[q])
+                       : "memory");
+        }
+        ptx::mbar_arrive(ctx.hand_full);
+        return;
+      }
+      topk_scan(p, taddr, 0, kHalf, e_lo, e_hi, lrow, bv, bi);
+      if (!ptx::mbar_wait(ctx.hand_full, parity, ctx.abort, ctx.wait_ns)) {
+        ctx.failed = true;
+        return;
+      }
+      float cv[kMaxTopK];
+      int ci[kMaxTopK];
+#pragma unroll
+      for (int q = 0; q < kMaxTopK; ++q) {
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cv[q]) : "r"(vbuf + static_cast<uint32_t>((q * kBM + r) * 4))
+                     : "memory");
+        asm volatile("ld.shared.s32 %0, [%1];" : "=r"(ci[q]) : "r"(ibuf + static_cast<uint32_t>((q * kBM + r) * 4))
+                     : "memory");
+      }
+      ptx::mbar_arrive(ctx.hand_free);
+#pragma unroll
+      for (int q = 0; q < kMaxTopK; ++q)
+        if (ci[q] >= 0 && cv[q] > bv[kMaxTopK - 1]) topk_insert(bv, bi, cv[q], ci[q]);
+    }
+    if (!valid) return;
+    write_topk(p, row, bv, bi);
   }
 };
 

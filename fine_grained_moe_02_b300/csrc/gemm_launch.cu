@@ -47,7 +47,7 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
   }
   if ((GW > 0) != (shape.a_gather != nullptr)) return MOE_ERR_UNSUPPORTED_SHAPE;  // gathered A needs gather warps
   auto kern = gemm_tc_kernel<BN, Epi, CL, GW>;
-  constexpr int kThreads = kGemmThreads + 32 * GW;
+  constexpr int kThreads = gemm_threads<Epi, GW>();
   // once per device: later calls (and stream captures) launch without it
   static std::atomic<uint64_t> smem_set{0};
   if (!smem_attr_ready(kern, S::kDynBytes, smem_set)) return MOE_ERR_CUDA;
@@ -65,7 +65,7 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = S::kDynBytes;
     cfg.stream = stream;
     cfg.attrs = attr;

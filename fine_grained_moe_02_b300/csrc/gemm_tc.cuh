@@ -41,7 +41,14 @@ constexpr int kBM = 128;          // tile rows (UMMA M)
 constexpr int kBK = 64;           // k per stage: one 128-byte swizzle row of bf16
 constexpr int kUK = 16;           // k per tcgen05.mma (kind::f16)
 constexpr int kMaxGroups = kMaxGemmGroups;  // tile prefix table in shared memory
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 192;  // producer + MMA warps and four epilogue warps
+
+// Threads of a GEMM CTA: producer and MMA warps, Epi::kWarps epilogue warps
+// (4, or 8 when two warps share each TMEM lane quadrant) and GW gather warps.
+template <class Epi, int GW>
+constexpr int gemm_threads() {
+  return 64 + 32 * Epi::kWarps + 32 * GW;
+}
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kOutChunkBytes = 32 * 128;          // 32 rows x 64 bf16
 
@@ -107,6 +114,16 @@ struct EpiCtx {
   bool pending;     // lane 0 has a committed bulk store that may still read `stage`
   uint32_t tempty;  // shared address of the current accumulator's "empty" barrier
   bool released;    // this warp has already arrived on `tempty` for the current tile
+  int part;         // with 8 epilogue warps: which of the quadrant's two warps (0, 1)
+  uint32_t scratch; // shared address of the epilogue scratch (the staging area)
+  // hand-off between a quadrant's two warps (8 epilogue warps): "filled" and
+  // "free" mbarriers of the quadrant (32 arrivals each), uses so far, and the
+  // bounds of every wait; `failed` reports a wait that ran out
+  uint32_t hand_full, hand_free;
+  uint32_t hand_uses;
+  const volatile int* abort;
+  uint64_t wait_ns;
+  bool failed;
 };
 
 struct TileCoord {
@@ -151,7 +168,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GroupRows& rows
 //                                                 int row_in_tile, EpiCtx&);
 // taddr addresses this thread's lane (= tile row) at the accumulator's column 0.
 template <int BN, class Epi, int CL = 1, int GW = 0>
-__global__ void __launch_bounds__(kGemmThreads + 32 * GW, 1)
+__global__ void __launch_bounds__(gemm_threads<Epi, GW>(), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d, GemmShape shape, typename Epi::Params ep) {
   using S = GemmSmem<BN>;
@@ -164,6 +181,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t hand_bar[8];  // 8 epilogue warps: per quadrant "filled" (0-3) and "free" (4-7)
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_tile[kMaxGroups + 1];
@@ -171,7 +189,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ int s_bad;
 
   static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
-  static_assert(GW == 0 || (CL == 1 && kBM % (4 * GW) == 0), "gather warps: single CTAs");
+  static_assert(GW == 0 || (CL == 1 && kBM % (4 * (GW > 0 ? GW : 1)) == 0), "gather warps: single CTAs");
   static_assert(kGatherLag < STAGES, "a gather thread must be able to issue past the stage it signals");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -231,9 +249,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
-      ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 128);
+      ptx::mbar_init(ptx::smem_u32(&tempty_bar[b]), 32 * Epi::kWarps);
     }
     ptx::mbar_init(ptx::smem_u32(&drain_bar), 1);
+    for (int q = 0; q < 8; ++q) ptx::mbar_init(ptx::smem_u32(&hand_bar[q]), 32);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -256,9 +275,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   const int num_kb = shape.K / kBK;
   const uint64_t wait_ns = shape.wait_limit_ns ? shape.wait_limit_ns : kWaitLimitNs;
 
-  if (GW > 0 && warp >= kGemmThreads / 32) {
+  constexpr int kEpiEnd = 2 + Epi::kWarps;  // first warp after the epilogue warps
+  static_assert(Epi::kWarps == 4 || Epi::kWarps == 8, "one or two epilogue warps per TMEM lane quadrant");
+  if (GW > 0 && warp >= kEpiEnd) {
     // -------------------------------------------------------- A gather warps
-    const int gt = static_cast<int>(threadIdx.x) - kGemmThreads;  // 0 .. 32*GW - 1
+    const int gt = static_cast<int>(threadIdx.x) - 32 * kEpiEnd;  // 0 .. 32*GW - 1
     constexpr int kRowStep = 4 * (GW > 0 ? GW : 1);               // rows per instruction of all gather warps
     constexpr int kRowsPer = kBM / kRowStep;                      // rows per thread per k-slice
     const int chunk = gt & 7;                                     // this lane's 16-byte chunk of a row slice
@@ -423,7 +444,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     EpiCtx ctx{&tmap_d, ptx::smem_u32(smem + STAGES * S::kStageBytes + quad * kOutChunkBytes), lane, quad, false,
-               0u, false};
+               0u, false, (warp - 2) / 4, ptx::smem_u32(smem + STAGES * S::kStageBytes),
+               ptx::smem_u32(&hand_bar[quad]), ptx::smem_u32(&hand_bar[4 + quad]), 0u, &s_abort, wait_ns, false};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = first_tile; tile < total; tile += tile_step) {
@@ -440,6 +462,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       // an epilogue may hand the accumulator back itself (release_accumulator)
       // as soon as it holds the tile in registers, before its stores
       Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile, ctx);
+      if (__any_sync(0xffffffffu, ctx.failed)) {
+        if (lane == 0) atomicOr(shape.status, MOE_DEV_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
       if (!ctx.released) {
         ptx::tc_fence_before();
         ptx::mbar_arrive(ctx.tempty);
