@@ -285,8 +285,20 @@ def measure_headlocal_variant(torch, moe, steps: int) -> dict:
         raise SystemExit("device status set by moe_forward_headlocal")
     ms = e0.elapsed_time(e1) / steps
     flops = cfg.T * cfg.n_heads * (2 * cfg.head_dim * cfg.E + 6 * cfg.top_k * cfg.head_dim * cfg.inter)
+    # the layer is bound by HBM: every head-local expert's weights are streamed
+    # once for few rows each, and x_perm, act and y_perm each go out and back
+    H, Dh, E, I, T = cfg.n_heads, cfg.head_dim, cfg.E, cfg.inter, cfg.T
+    Tk = T * cfg.top_k
+    alg_bytes = (2 * T * cfg.d * 2 + H * E * Dh * 2          # x (router, gather), router weights
+                 + H * Tk * 8                                 # indices + gates
+                 + H * E * (2 * I * Dh + Dh * I) * 2          # expert weights
+                 + 2 * H * Tk * Dh * 2 + 2 * H * Tk * I * 2   # x_perm, act: written and read
+                 + 2 * H * Tk * Dh * 2 + T * cfg.d * 2)       # y_perm written and read, out
+    hbm = peaks()["hbm"]
     return {"workload": cfg.note, "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "layer_tflops": flops / (ms * 1e-3) / 1e12,
+            "algorithmic_bytes": alg_bytes, "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+            "frac_hbm": alg_bytes / (ms * 1e-3) / 1e9 / hbm,
             "path": "moe_forward_headlocal: all heads' routers + top-k as one batched GEMM, one sort and gather "
                     "over (head, token), grouped SwiGLU GEMMs head by head, one combine into each head's columns"}
 

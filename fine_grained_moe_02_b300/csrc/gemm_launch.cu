@@ -32,57 +32,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-template <int BN, class Epi, int CL = 1, int GW = 0>
+template <int BN, class Epi, int GW = 0>
 int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const GemmShape& shape,
              const typename Epi::Params& ep, int grid, cudaStream_t stream, int b_box_rows) {
   using S = GemmSmem<BN>;
   // the B tensor map must deliver exactly this kernel's per-CTA B slice, or
   // the stage byte count and the shared-memory ring would disagree
-  if (b_box_rows != BN / CL) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (b_box_rows != BN) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (shape.groups < 1 || shape.groups > kMaxGroups) return MOE_ERR_UNSUPPORTED_SHAPE;  // shared tile table
   {  // the kernel counts tiles in 32-bit ints: at most (rows / tile rows + groups) m-tiles per n-tile
     const int64_t rows_all = shape.batched ? static_cast<int64_t>(shape.groups) * shape.M : shape.M;
-    const int64_t m_tiles = rows_all / (CL * kBM) + shape.groups;
+    const int64_t m_tiles = rows_all / kBM + shape.groups;
     if (shape.N % BN != 0 || m_tiles * (shape.N / BN) >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   }
   if ((GW > 0) != (shape.a_gather != nullptr)) return MOE_ERR_UNSUPPORTED_SHAPE;  // gathered A needs gather warps
-  auto kern = gemm_tc_kernel<BN, Epi, CL, GW>;
+  auto kern = gemm_tc_kernel<BN, Epi, GW>;
   constexpr int kThreads = gemm_threads<Epi, GW>();
   // once per device: later calls (and stream captures) launch without it
   static std::atomic<uint64_t> smem_set{0};
   if (!smem_attr_ready(kern, S::kDynBytes, smem_set)) return MOE_ERR_CUDA;
   if (grid < 1) grid = 1;
-  if constexpr (CL == 1) {
-    kern<<<grid, kThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-  } else {
-    // Persistent grid of CTA pairs: never more pairs than can be resident at
-    // once (every CTA must be running for the static tile schedule to finish
-    // in one wave of CTAs).
-    cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = S::kDynBytes;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int max_clusters = 0;  // per process; the same part everywhere this runs
-    if (max_clusters == 0) {
-      cfg.gridDim = dim3(2 * 148);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
-      max_clusters = n;
-    }
-    int pairs = (grid + 1) / 2;
-    if (pairs > max_clusters) pairs = max_clusters;
-    cfg.gridDim = dim3(2 * pairs);
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, td, shape, ep) != cudaSuccess) return MOE_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-  }
+  kern<<<grid, kThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <class Epi>
@@ -99,13 +70,6 @@ int run_gemm_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   }
 }
 
-// CTA pairs (clusters of two sharing the B tile by TMA multicast, CL = 2 in
-// gemm_tc.cuh) cut L2-to-SM traffic by a third but were measured slower on
-// B300: clip workload 17.58 vs 17.43 ms per layer (expert GEMM-1 8.40 vs
-// 8.11 ms; GEMM-2 4.63 vs 4.73 ms), slice workload GEMM-1 361 vs 322 us (odd
-// m-block counts add empty partner tiles).  The GEMMs are power-bound, not
-// L2-bound, at full size.  Kept available, off.
-constexpr bool kUseCtaPairs = false;
 
 int pick_bn(int n) {
   if (n % 256 == 0) return 256;
@@ -143,16 +107,14 @@ int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb, td;
   {
     const int bn = pick_bn(a.L);
-    const bool pair = kUseCtaPairs && (bn == 256);  // CTA pairs share the W_lat tile (multicast)
     if (!make_tmap_bf16_2d(&ta, a.x, a.d, a.T, kBK, kBM)) return MOE_ERR_CUDA;
-    if (!make_tmap_bf16_2d(&tb, a.w_lat, a.d, a.L, kBK, pair ? bn / 2 : bn)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&tb, a.w_lat, a.d, a.L, kBK, bn)) return MOE_ERR_CUDA;
     if (!make_tmap_bf16_2d(&td, a.hl, 2ULL * a.L, a.T, kBK, 32)) return MOE_ERR_CUDA;
     GemmShape sh{a.d, a.d, a.L, 1, nullptr, static_cast<int>(a.T), a.status};
     EpiHiLo::Params ep{a.hl, 2LL * a.L, a.L};
     const int64_t tiles = m_tiles * (a.L / bn);
     const int grid = static_cast<int>(tiles < a.sm_count ? tiles : a.sm_count);
-    const int rc = pair ? run_gemm<256, EpiHiLo, 2>(ta, tb, td, sh, ep, grid, stream, bn / 2)
-                        : run_gemm_bn<EpiHiLo>(bn, ta, tb, td, sh, ep, grid, stream, bn);
+    const int rc = run_gemm_bn<EpiHiLo>(bn, ta, tb, td, sh, ep, grid, stream, bn);
     if (rc != MOE_OK) return rc;
   }
   {
@@ -212,14 +174,11 @@ int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
   const int rows = static_cast<int>(a.rows);
   const int n = 2 * a.I;
   const int bn = (n % 256 == 0) ? 256 : 128;
-  const bool pair = kUseCtaPairs && (bn == 256);  // CTA pairs share the w13 tile (multicast)
   if (!make_tmap_bf16_2d(&ta, a.x_perm, a.d, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
-  if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, pair ? bn / 2 : bn))
-    return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, a.w13, a.d, static_cast<uint64_t>(a.E) * n, kBK, bn)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&td, a.act, a.I, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status};
   EpiSwiGLU::Params ep{a.act, a.I};
-  if (pair) return run_gemm<256, EpiSwiGLU, 2>(ta, tb, td, sh, ep, a.sm_count, stream, bn / 2);
   return (bn == 256) ? run_gemm<256, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn)
                      : run_gemm<128, EpiSwiGLU>(ta, tb, td, sh, ep, a.sm_count, stream, bn);
 }
@@ -239,8 +198,8 @@ int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream) {
   sh.a_src = a.x;
   sh.a_ld = a.d;
   EpiSwiGLU::Params ep{a.act, a.I};
-  return (bn == 256) ? run_gemm<256, EpiSwiGLU, 1, 2>(tb, tb, td, sh, ep, a.sm_count, stream, bn)
-                     : run_gemm<128, EpiSwiGLU, 1, 2>(tb, tb, td, sh, ep, a.sm_count, stream, bn);
+  return (bn == 256) ? run_gemm<256, EpiSwiGLU, 2>(tb, tb, td, sh, ep, a.sm_count, stream, bn)
+                     : run_gemm<128, EpiSwiGLU, 2>(tb, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
 // Expert GEMM-2 over ragged groups: y_perm = act Wd^T.
@@ -248,15 +207,12 @@ int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb, td;
   const int rows = static_cast<int>(a.rows);
   const int bn = pick_bn(a.d);
-  const bool pair = kUseCtaPairs && (bn == 256);  // CTA pairs share the w_down tile (multicast)
   if (!make_tmap_bf16_2d(&ta, a.act, a.I, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
-  if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, pair ? bn / 2 : bn))
-    return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, bn)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&td, a.y_perm, a.d, a.rows, kBK, 32)) return MOE_ERR_CUDA;
   GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
   EpiStoreBf16::Params ep{a.y_perm, a.d};
-  return pair ? run_gemm<256, EpiStoreBf16, 2>(ta, tb, td, sh, ep, a.sm_count, stream, bn / 2)
-              : run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream, bn);
+  return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
 // Self-test of the bounded waits: one 128 x 256 x 64 tile whose producer

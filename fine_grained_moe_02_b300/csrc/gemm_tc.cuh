@@ -15,13 +15,6 @@
 // (tile = blockIdx.x + i * gridDim.x) in group-major, m-major, n-minor order
 // so that CTAs running at the same time share A and B tiles through L2.
 //
-// CL = 2 (cluster of two CTAs on adjacent m-blocks of the same group and
-// n-tile): each CTA loads its own A rows and one half of the shared B tile,
-// multicasting that half into both CTAs' shared memory, so the pair reads B
-// from L2 once (a third less L2-to-SM traffic per tile).  Each CTA's MMA
-// commit frees the stage in both CTAs.  A group with an odd number of
-// m-blocks pairs its last one with an empty partner (computed, never stored).
-//
 // Every wait is bounded (see ptx::mbar_wait): on a timeout the kernel sets
 // MOE_DEV_TIMEOUT in the status word, the other roles stop, in-flight TMA
 // loads and MMAs are drained (again with a limit), TMEM is freed and the
@@ -145,7 +138,7 @@ struct GroupRows {
 
 template <int BN>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GroupRows& rows, const int* s_tile, int groups,
-                                                 int n_tiles, int cl = 1, int crank = 0) {
+                                                 int n_tiles) {
   // largest g with s_tile[g] <= tile
   int lo = 0, hi = groups - 1;
   while (lo < hi) {
@@ -157,7 +150,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GroupRows& rows
   const int local = tile - s_tile[lo];
   c.m_blk = local / n_tiles;
   c.n_blk = local - c.m_blk * n_tiles;
-  c.row0 = rows(lo) + (c.m_blk * cl + crank) * kBM;
+  c.row0 = rows(lo) + c.m_blk * kBM;
   c.row_end = rows(lo + 1);
   return c;
 }
@@ -167,7 +160,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GroupRows& rows
 //   template <int BN> static __device__ void run(const Params&, const TileCoord&, uint32_t taddr,
 //                                                 int row_in_tile, EpiCtx&);
 // taddr addresses this thread's lane (= tile row) at the accumulator's column 0.
-template <int BN, class Epi, int CL = 1, int GW = 0>
+template <int BN, class Epi, int GW = 0>
 __global__ void __launch_bounds__(gemm_threads<Epi, GW>(), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                const __grid_constant__ CUtensorMap tmap_d, GemmShape shape, typename Epi::Params ep) {
@@ -188,17 +181,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ int s_total;
   __shared__ int s_bad;
 
-  static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
-  static_assert(GW == 0 || (CL == 1 && kBM % (4 * (GW > 0 ? GW : 1)) == 0), "gather warps: single CTAs");
+  static_assert(kBM % (4 * (GW > 0 ? GW : 1)) == 0, "gather warps cover the tile's rows evenly");
   static_assert(kGatherLag < STAGES, "a gather thread must be able to issue past the stage it signals");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = shape.N / BN;
   const int groups = shape.groups;
-  const int crank = CL == 2 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
-  const int first_tile = CL == 2 ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
-  const int tile_step = CL == 2 ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
-  constexpr uint16_t kPair = 0x3;
+  const int first_tile = static_cast<int>(blockIdx.x);
+  const int tile_step = static_cast<int>(gridDim.x);
 
   // ---- group table: tile counts of the groups (all threads; group rows come
   // from the offsets in global memory, and again when a tile is decoded),
@@ -215,7 +205,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const int a = rows(g), b = rows(g + 1);
     int cnt = 0;
     if (a < 0 || b < a || b > row_limit) s_bad = 1;
-    else cnt = ((b - a + CL * kBM - 1) / (CL * kBM)) * n_tiles;
+    else cnt = ((b - a + kBM - 1) / kBM) * n_tiles;
     s_tile[g] = cnt;
   }
   __syncthreads();
@@ -245,7 +235,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1 + 32 * GW);  // the B (+A) loader, every gather thread
-      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), CL);  // every CTA's MMA frees the stage in all CTAs
+      ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_u32(&tfull_bar[b]), 1);
@@ -266,8 +256,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   }
   ptx::tc_fence_before();
   __syncthreads();
-  // the peer's barriers must be initialised before any multicast reaches them
-  if constexpr (CL == 2) ptx::cluster_sync();
   ptx::tc_fence_after();
 
   const uint32_t tmem_base = s_tmem;
@@ -349,7 +337,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       uint32_t last_par = 0;     // bit s: parity of the last fill of stage s
       bool ok = true;
       for (int tile = first_tile; tile < total && ok && !shape.selftest_stall; tile += tile_step) {
-        const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles, CL, crank);
+        const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
         const int b_row = c.group * (shape.b_group_rows ? shape.b_group_rows : shape.N) + c.n_blk * BN;
         const int a_row = shape.batched ? c.row0 - c.group * shape.M : c.row0;
         const int a_col = shape.batched ? c.group * shape.a_col_stride : 0;
@@ -365,13 +353,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
           const int k = kb * kBK;
           if (GW == 0)
             ptx::tma_load_2d(sa, &tmap_a, a_col + (shape.K_A > 0 ? k % shape.K_A : k), a_row, fb, pol_a);
-          if constexpr (CL == 2) {  // this CTA's half of B, into both CTAs
-            constexpr int kHalf = BN / 2;
-            ptx::tma_load_2d_multicast(sb + crank * kHalf * 128, &tmap_b, k % shape.K_B, b_row + crank * kHalf, fb,
-                                       kPair, pol_b);
-          } else {
-            ptx::tma_load_2d(sb, &tmap_b, k % shape.K_B, b_row, fb, pol_b);
-          }
+          ptx::tma_load_2d(sb, &tmap_b, k % shape.K_B, b_row, fb, pol_b);
           filled |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -420,8 +402,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             const uint64_t db = ptx::sw128_desc(sb + kk * kUK * 2);
             ptx::mma_bf16(d_tmem, da, db, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          if constexpr (CL == 2) ptx::mma_commit_multicast(ptx::smem_u32(&empty_bar[stage]), kPair);
-          else ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
+          ptx::mma_commit(ptx::smem_u32(&empty_bar[stage]));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -456,7 +437,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         break;
       }
       ptx::tc_fence_after();
-      const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles, CL, crank);
+      const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
       ctx.tempty = ptx::smem_u32(&tempty_bar[acc]);
       ctx.released = false;
       // an epilogue may hand the accumulator back itself (release_accumulator)
@@ -485,9 +466,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, S::kTmemCols);
   }
-  // neither CTA may exit while its peer can still multicast into it or
-  // arrive on its barriers
-  if constexpr (CL == 2) ptx::cluster_sync();
 }
 
 }  // namespace moe
