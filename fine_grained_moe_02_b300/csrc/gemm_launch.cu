@@ -184,7 +184,7 @@ int launch_gemm1(const FfnArgs& a, cudaStream_t stream) {
 }
 
 // Expert GEMM-1 with the row gather fused into the A loads: A row r is
-// x[src_token[r]], fetched four rows at a time by TMA tile::gather4, so the
+// x[src_token[r]], copied by two gather warps with 16-byte cp.async, so the
 // permuted copy x_perm never exists.
 int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream) {
   // A rows come from x through src_token (cp.async gather warps); tmap_a is unused

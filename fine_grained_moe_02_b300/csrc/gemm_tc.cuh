@@ -6,10 +6,12 @@
 //      the k coordinate of B is k mod K_B (lets one B serve a K = c*K_B sweep)
 //   groups: device offsets[G + 1]; group g owns A rows [offsets[g], offsets[g+1])
 //
-// One CTA per SM, 192 threads:
+// One CTA per SM, 64 + 32 * Epi::kWarps (+ 32 * GW) threads:
 //   warp 0       TMA producer (one lane): fills a STAGES-deep shared-memory ring
 //   warp 1       MMA issuer (one lane) and TMEM owner: tcgen05.mma 128 x BN x 16
-//   warps 2..5   epilogue: tcgen05.ld the accumulator, apply Epi, store to HBM
+//   warps 2..    epilogue (4 or 8 warps: warp w reads TMEM lane quadrant w % 4):
+//                tcgen05.ld the accumulator, apply Epi, store to HBM
+//   last GW      A gather warps (GW > 0): cp.async row copies instead of TMA
 // The accumulator is double-buffered in TMEM so the epilogue of tile i
 // overlaps the main loop of tile i+1.  Tiles are handed out statically
 // (tile = blockIdx.x + i * gridDim.x) in group-major, m-major, n-minor order
