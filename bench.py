@@ -164,9 +164,14 @@ class Clocks:
 
 
 def gemm_src_hash() -> str:
+    """Hash of the GEMM engine's code (comments and blank lines left out), so
+    that a traffic capture stays attached to the kernel it measured."""
     h = hashlib.sha256()
     for n in GEMM_SOURCES:
-        h.update((ROOT / "fine_grained_moe_02_b300" / "csrc" / n).read_bytes())
+        for line in (ROOT / "fine_grained_moe_02_b300" / "csrc" / n).read_text().splitlines():
+            code = line.split("//", 1)[0].rstrip() if not line.lstrip().startswith("#include") else line.rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
