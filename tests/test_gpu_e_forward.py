@@ -103,7 +103,8 @@ def test_forward_host_chunks_match_one_forward(T, pinned):
 
 
 @pytest.mark.parametrize("kw", [dict(T=3000, d=512, E=32, inter=256), dict(T=77, d=4096, E=8, inter=1024),
-                                dict(T=1, d=512, E=16, inter=128)])
+                                dict(T=1, d=512, E=16, inter=128),
+                                dict(T=500, d=256, E=8, inter=192)])   # 2*inter = 384: 128-wide N tiles
 def test_gathered_gemm1_equals_gemm1_on_x_perm(kw):
     inp = G.small_inputs(**kw)
     dev = G.Dev(inp)
