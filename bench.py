@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=512, help="tokens in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--variant", choices=["headlocal", "ext"], default=None,
+                    help="time one widened variant alone (its JSON entry only; for profiling)")
     return ap.parse_args()
 
 
@@ -363,6 +365,15 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    if args.variant is not None:  # one variant alone, on this rank's GPU
+        fn = measure_headlocal_variant if args.variant == "headlocal" else measure_ext_variant
+        line = fn(torch, moe, max(3, args.steps))
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     cfg = mi.CONFIGS[args.workload]
     inp = mi.make_weights(cfg)
