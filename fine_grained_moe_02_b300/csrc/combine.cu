@@ -1,6 +1,9 @@
 // Gate-weighted combine: out[t] = sum_s gate[t,s] * y_perm[row_of[t,s]].
 // One warp per token, scatter-free (each output row has one writer), fp32
 // accumulation in slot order, one bf16 rounding.  16-byte vector loads.
+// Follows the last step of the MagiMoE operator library's routing -> sorting ->
+// calculation chain ("Sand.ai: The world's first 100-billion-parameter open-source MoE video generation model MAGI Preview" (36kr), section "02. Two Key Technical Decision Points"):
+// the routed experts' outputs are brought back to token order and summed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>

@@ -1,5 +1,6 @@
 // Sorting stage: counting-sort permutation of the (token, slot) pairs into
 // expert-contiguous order, and the row gather x -> x_perm.
+// This is the "sorting" step of the MagiMoE operator library ("Sand.ai: The world's first 100-billion-parameter open-source MoE video generation model MAGI Preview" (36kr), section "02. Two Key Technical Decision Points").
 //
 //   1. hist    : per token block, per-expert counts            (blocks of kTokBlock tokens)
 //   2. scan    : per expert, exclusive prefix over blocks; offsets = exclusive prefix

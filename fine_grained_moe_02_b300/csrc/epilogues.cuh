@@ -1,4 +1,6 @@
-// Epilogues of the tcgen05 GEMM engine.  Each thread owns one accumulator
+// Epilogues of the tcgen05 GEMM engine: the router's hi/lo split and top-6
+// selection ("MAGI-2 Preview" (heyaiwiki), Architecture table, "Routing" row), the
+// experts' SwiGLU and the plain bf16 store.  Each thread owns one accumulator
 // row (its TMEM lane); a warp owns 32 consecutive rows of the tile.  Results
 // leave through a per-warp 32-row x 64-column staging chunk in shared memory
 // (128-byte swizzled, the layout the output tensor map uses) and one TMA bulk

@@ -1,5 +1,9 @@
 // Host launchers for the tcgen05 GEMM engine: the two router GEMMs and the
 // two grouped expert GEMMs, plus the tensor-map encoder and the w13 builder.
+// The router is the multi-head latent routing of "MAGI-2 Preview" (heyaiwiki), Architecture
+// table ("Architecture" and "Routing" rows: 12 latent heads x 256, top-6);
+// the expert GEMMs are the "calculation" step over many small matrices of
+// "Sand.ai: The world's first 100-billion-parameter open-source MoE video generation model MAGI Preview" (36kr), section "02. Two Key Technical Decision Points".
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

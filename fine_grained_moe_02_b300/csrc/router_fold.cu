@@ -4,6 +4,8 @@
 // (A = [x | x], B = w_router).  The summed head scores are linear in x, so
 // this is the same function as latent projection followed by head scores.
 // One-time preparation per weight load: a plain fp32 SIMT GEMM.
+// The routing it computes is the multi-head latent routing of "MAGI-2 Preview" (heyaiwiki),
+// Architecture table, "Routing" row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>

@@ -1,5 +1,7 @@
 // Fused router: latent projection, summed head scores, softmax and top-k in
-// one persistent tcgen05 kernel.  The latent vector h never leaves the SM:
+// one persistent tcgen05 kernel (the multi-head latent routing of
+// "MAGI-2 Preview" (heyaiwiki), Architecture table, "Routing" row and FAQ "What is
+// MagiMoE?").  The latent vector h never leaves the SM:
 // per 128-token tile and per head j,
 //   1. h_j = x W_lat[j]^T accumulates in TMEM columns [0, head_dim) (fp32),
 //   2. the epilogue warps read it back 64 columns at a time and write the bf16
