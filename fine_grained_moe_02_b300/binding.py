@@ -150,6 +150,42 @@ def _ptr(t) -> ctypes.c_void_p | None:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _need(dims, **tensors) -> None:
+    """Each named tensor must hold at least the elements its role needs for
+    `dims` (the C ABI takes bare pointers and cannot check this; a short
+    buffer would be read or written past its end on the device)."""
+    T, d, E, I, k = int(dims.T), int(dims.d), int(dims.E), int(dims.inter), int(dims.top_k)
+    H, Dh = int(dims.n_heads), int(dims.head_dim)
+    L = H * Dh
+    sizes = {
+        "x": T * d, "out": T * d, "x_host": T * d, "out_host": T * d,
+        "w_lat": L * d, "w_head": E * L, "bias": E, "w_router": E * 2 * d,
+        "topk_idx": T * k, "topk_gate": T * k, "logits": T * E,
+        "w_gate": E * I * d, "w_up": E * I * d, "w13": E * 2 * I * d, "w_down": E * d * I,
+        "offsets": E + 1, "row_of": T * k, "src_token": T * k,
+        "x_perm": T * k * d, "y_perm": T * k * d, "act": T * k * I, "status": 1,
+    }
+    for name, t in tensors.items():
+        if t is None or isinstance(t, int):
+            continue
+        need = sizes[name]
+        if t.numel() < need:
+            raise ValueError(f"{name}: {t.numel()} elements, these dims need {need}")
+
+
+def _need_n(**named) -> None:
+    """name=(tensor, elements needed) pairs, for layouts _need does not cover."""
+    for name, (t, need) in named.items():
+        if t is not None and not isinstance(t, int) and t.numel() < need:
+            raise ValueError(f"{name}: {t.numel()} elements, these dims need {need}")
+
+
+def _ext_dims(dims, ext):
+    """dims with the shared experts added: E + n_shared experts, top_k + n_shared slots."""
+    return moe_dims.make(dims.T, dims.d, dims.E + ext.n_shared, dims.inter, dims.top_k + ext.n_shared,
+                         dims.n_heads, dims.head_dim)
+
+
 def _dev(*ts, dtype=None) -> None:
     for t in ts:
         if t is None:
@@ -211,12 +247,14 @@ def moe_selftest_timeout(ws, limit_us: int, stream=None) -> None:
 
 
 def moe_prepare_weights(dims, w_gate, w_up, w13, stream=None) -> None:
+    _need(dims, w_gate=w_gate, w_up=w_up, w13=w13)
     _dev(w_gate, w_up, w13, dtype=torch.bfloat16)
     _check(lib().moe_prepare_weights(ctypes.byref(dims), _ptr(w_gate), _ptr(w_up), _ptr(w13), _stream(stream)),
            "moe_prepare_weights")
 
 
 def moe_route(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, topk_idx=topk_idx, topk_gate=topk_gate, logits=logits)
     _dev(x, w_lat, w_head, dtype=torch.bfloat16)
     _dev(bias, topk_gate, logits, dtype=torch.float32)
     _dev(topk_idx, dtype=torch.int32)
@@ -225,6 +263,7 @@ def moe_route(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, str
 
 
 def moe_route_fused(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, topk_idx=topk_idx, topk_gate=topk_gate, logits=logits)
     _dev(x, w_lat, w_head, dtype=torch.bfloat16)
     _dev(bias, topk_gate, logits, dtype=torch.float32)
     _dev(topk_idx, dtype=torch.int32)
@@ -234,12 +273,14 @@ def moe_route_fused(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, w
 
 
 def moe_prepare_router(dims, w_lat, w_head, w_router, stream=None) -> None:
+    _need(dims, w_lat=w_lat, w_head=w_head, w_router=w_router)
     _dev(w_lat, w_head, w_router, dtype=torch.bfloat16)
     _check(lib().moe_prepare_router(ctypes.byref(dims), _ptr(w_lat), _ptr(w_head), _ptr(w_router), _stream(stream)),
            "moe_prepare_router")
 
 
 def moe_route_folded(dims, x, w_router, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _need(dims, x=x, w_router=w_router, bias=bias, topk_idx=topk_idx, topk_gate=topk_gate, logits=logits)
     _dev(x, w_router, dtype=torch.bfloat16)
     _dev(bias, topk_gate, logits, dtype=torch.float32)
     _dev(topk_idx, dtype=torch.int32)
@@ -249,6 +290,7 @@ def moe_route_folded(dims, x, w_router, bias, topk_idx, topk_gate, logits, ws, s
 
 
 def moe_forward_folded(dims, x, w_router, bias, w13, w_down, out, ws, stream=None) -> None:
+    _need(dims, x=x, w_router=w_router, bias=bias, w13=w13, w_down=w_down, out=out)
     _dev(x, w_router, w13, w_down, out, dtype=torch.bfloat16)
     _dev(bias, dtype=torch.float32)
     _check(lib().moe_forward_folded(ctypes.byref(dims), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w13),
@@ -257,6 +299,7 @@ def moe_forward_folded(dims, x, w_router, bias, w13, w_down, out, ws, stream=Non
 
 
 def moe_dispatch(dims, x, topk_idx, offsets, row_of, src_token, x_perm, ws, stream=None) -> None:
+    _need(dims, x=x, topk_idx=topk_idx, offsets=offsets, row_of=row_of, src_token=src_token, x_perm=x_perm)
     _dev(x, x_perm, dtype=torch.bfloat16)
     _dev(topk_idx, offsets, row_of, src_token, dtype=torch.int32)
     _check(lib().moe_dispatch(ctypes.byref(dims), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
@@ -264,12 +307,14 @@ def moe_dispatch(dims, x, topk_idx, offsets, row_of, src_token, x_perm, ws, stre
 
 
 def moe_dispatch_indices(dims, topk_idx, offsets, row_of, src_token, ws, stream=None) -> None:
+    _need(dims, topk_idx=topk_idx, offsets=offsets, row_of=row_of, src_token=src_token)
     _dev(topk_idx, offsets, row_of, src_token, dtype=torch.int32)
     _check(lib().moe_dispatch_indices(ctypes.byref(dims), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),
                                       _ptr(src_token), _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch_indices")
 
 
 def moe_expert_gemm1_gather(dims, x, src_token, offsets, w13, act, ws, stream=None) -> None:
+    _need(dims, x=x, src_token=src_token, offsets=offsets, w13=w13, act=act)
     _dev(x, w13, act, dtype=torch.bfloat16)
     _dev(src_token, offsets, dtype=torch.int32)
     _check(lib().moe_expert_gemm1_gather(ctypes.byref(dims), _ptr(x), _ptr(src_token), _ptr(offsets), _ptr(w13),
@@ -277,6 +322,7 @@ def moe_expert_gemm1_gather(dims, x, src_token, offsets, w13, act, ws, stream=No
 
 
 def moe_dispatch_noalloc(dims, x, topk_idx, offsets, row_of, src_token, x_perm, status=None, stream=None) -> None:
+    _need(dims, x=x, topk_idx=topk_idx, offsets=offsets, row_of=row_of, src_token=src_token, x_perm=x_perm, status=status)
     """moe_dispatch without a workspace (scratch in a fixed array inside libmoe)."""
     _dev(x, x_perm, dtype=torch.bfloat16)
     _dev(topk_idx, offsets, row_of, src_token, status, dtype=torch.int32)
@@ -286,6 +332,7 @@ def moe_dispatch_noalloc(dims, x, topk_idx, offsets, row_of, src_token, x_perm, 
 
 
 def moe_expert_ffn(dims, x_perm, offsets, w13, w_down, act, y_perm, ws, stream=None) -> None:
+    _need(dims, x_perm=x_perm, offsets=offsets, w13=w13, w_down=w_down, act=act, y_perm=y_perm)
     _dev(x_perm, w13, w_down, act, y_perm, dtype=torch.bfloat16)
     _dev(offsets, dtype=torch.int32)
     _check(lib().moe_expert_ffn(ctypes.byref(dims), _ptr(x_perm), _ptr(offsets), _ptr(w13), _ptr(w_down),
@@ -293,6 +340,7 @@ def moe_expert_ffn(dims, x_perm, offsets, w13, w_down, act, y_perm, ws, stream=N
 
 
 def moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws, stream=None) -> None:
+    _need(dims, x_perm=x_perm, offsets=offsets, w13=w13, act=act)
     _dev(x_perm, w13, act, dtype=torch.bfloat16)
     _dev(offsets, dtype=torch.int32)
     _check(lib().moe_expert_gemm1(ctypes.byref(dims), _ptr(x_perm), _ptr(offsets), _ptr(w13), _ptr(act),
@@ -300,6 +348,7 @@ def moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws, stream=None) -> None:
 
 
 def moe_expert_gemm2(dims, act, offsets, w_down, y_perm, ws, stream=None) -> None:
+    _need(dims, act=act, offsets=offsets, w_down=w_down, y_perm=y_perm)
     _dev(act, w_down, y_perm, dtype=torch.bfloat16)
     _dev(offsets, dtype=torch.int32)
     _check(lib().moe_expert_gemm2(ctypes.byref(dims), _ptr(act), _ptr(offsets), _ptr(w_down), _ptr(y_perm),
@@ -307,6 +356,7 @@ def moe_expert_gemm2(dims, act, offsets, w_down, y_perm, ws, stream=None) -> Non
 
 
 def moe_combine(dims, y_perm, row_of, topk_gate, out, stream=None) -> None:
+    _need(dims, y_perm=y_perm, row_of=row_of, topk_gate=topk_gate, out=out)
     _dev(y_perm, out, dtype=torch.bfloat16)
     _dev(row_of, dtype=torch.int32)
     _dev(topk_gate, dtype=torch.float32)
@@ -315,6 +365,7 @@ def moe_combine(dims, y_perm, row_of, topk_gate, out, stream=None) -> None:
 
 
 def moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, w13=w13, w_down=w_down, out=out)
     _dev(x, w_lat, w_head, w13, w_down, out, dtype=torch.bfloat16)
     _dev(bias, dtype=torch.float32)
     _check(lib().moe_forward(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(w13),
@@ -329,6 +380,8 @@ def moe_workspace_size_ext(dims, ext) -> int:
 
 
 def moe_route_ext(dims, ext, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, logits=logits)
+    _need(_ext_dims(dims, ext), topk_idx=topk_idx, topk_gate=topk_gate)
     _dev(x, w_lat, w_head, dtype=torch.bfloat16)
     _dev(bias, topk_gate, logits, dtype=torch.float32)
     _dev(topk_idx, dtype=torch.int32)
@@ -338,6 +391,8 @@ def moe_route_ext(dims, ext, x, w_lat, w_head, bias, topk_idx, topk_gate, logits
 
 
 def moe_forward_ext(dims, ext, x, w_lat, w_head, bias, w13, w_down, out, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, out=out)
+    _need(_ext_dims(dims, ext), w13=w13, w_down=w_down)
     _dev(x, w_lat, w_head, w13, w_down, out, dtype=torch.bfloat16)
     _dev(bias, dtype=torch.float32)
     _check(lib().moe_forward_ext(ctypes.byref(dims), ctypes.byref(ext), _ptr(x), _ptr(w_lat), _ptr(w_head),
@@ -352,12 +407,18 @@ def moe_workspace_size_headlocal(dims) -> int:
 
 
 def moe_prepare_weights_headlocal(dims, w_gate, w_up, w13, stream=None) -> None:
+    H, E, Dh, I, T, k = dims.n_heads, dims.E, dims.head_dim, dims.inter, dims.T, dims.top_k
+    _need_n(w_gate=(w_gate, H * E * I * Dh), w_up=(w_up, H * E * I * Dh), w13=(w13, H * E * 2 * I * Dh))
     _dev(w_gate, w_up, w13, dtype=torch.bfloat16)
     _check(lib().moe_prepare_weights_headlocal(ctypes.byref(dims), _ptr(w_gate), _ptr(w_up), _ptr(w13),
                                                _stream(stream)), "moe_prepare_weights_headlocal")
 
 
 def moe_forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, logits, ws, stream=None) -> None:
+    H, E, Dh, I, T, k = dims.n_heads, dims.E, dims.head_dim, dims.inter, dims.T, dims.top_k
+    _need_n(x=(x, T * dims.d), w_router=(w_router, H * E * Dh), bias=(bias, H * E), w13=(w13, H * E * 2 * I * Dh),
+            w_down=(w_down, H * E * Dh * I), out=(out, T * dims.d), topk_idx=(topk_idx, H * T * k),
+            logits=(logits, H * T * E))
     _dev(x, w_router, w13, w_down, out, dtype=torch.bfloat16)
     _dev(bias, logits, dtype=torch.float32)
     _dev(topk_idx, dtype=torch.int32)
@@ -368,6 +429,8 @@ def moe_forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, l
 
 def moe_forward_host(dims, x_host, w_lat, w_head, bias, w13, w_down, out_host, ws, stream=None) -> None:
     """x_host/out_host: CPU bf16 tensors (pinned for full bandwidth); weights on the device."""
+    _need(dims, x_host=x_host, w_lat=w_lat, w_head=w_head, bias=bias, w13=w13, w_down=w_down,
+          out_host=out_host)
     if x_host.is_cuda or out_host.is_cuda:
         raise ValueError("x_host/out_host must be host tensors")
     _dev(w_lat, w_head, w13, w_down, dtype=torch.bfloat16)

@@ -103,3 +103,36 @@ def test_selftest_argument_checks(L):
     assert L.moe_selftest_timeout(P, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_timeout(ctypes.c_void_p(0x10008), 1 << 20, 1000, None) == B.MOE_ERR_MISALIGNED
     assert L.moe_selftest_timeout(P, 4096, 1000, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_undersized_tensors_are_rejected_before_any_device_work():
+    # the C ABI takes bare pointers; the binding checks every buffer against dims
+    import torch
+    d = moe.moe_dims.make(256, 512, 16, 128, top_k=2)
+    T, D, E, I, k, L = 256, 512, 16, 128, 2, 12 * 256
+    bf = lambda n: torch.zeros(n, dtype=torch.bfloat16)
+    ok = dict(x=bf(T * D), w_lat=bf(L * D), w_head=bf(E * L), w13=bf(E * 2 * I * D), w_down=bf(E * D * I),
+              out=bf(T * D))
+    for name in ok:
+        args = dict(ok)
+        args[name] = bf(ok[name].numel() - 1)
+        with pytest.raises(ValueError, match=name):
+            moe.moe_forward(d, args["x"], args["w_lat"], args["w_head"], None, args["w13"], args["w_down"],
+                            args["out"], torch.zeros(1, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="act"):
+        moe.moe_expert_gemm1(d, bf(T * k * D), torch.zeros(E + 1, dtype=torch.int32), bf(E * 2 * I * D),
+                             bf(T * k * I - 8), torch.zeros(1, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="offsets"):
+        moe.moe_dispatch(d, bf(T * D), torch.zeros(T * k, dtype=torch.int32), torch.zeros(E, dtype=torch.int32),
+                         torch.zeros(T * k, dtype=torch.int32), torch.zeros(T * k, dtype=torch.int32),
+                         bf(T * k * D), torch.zeros(1, dtype=torch.uint8))
+    # shared experts: w13 holds E + n_shared experts, the slots top_k + n_shared
+    ext = moe.moe_ext.make(n_shared=1)
+    with pytest.raises(ValueError, match="w13"):
+        moe.moe_forward_ext(d, ext, ok["x"], ok["w_lat"], ok["w_head"], None, ok["w13"], bf((E + 1) * D * I),
+                            ok["out"], torch.zeros(1, dtype=torch.uint8))
+    # head-local: per-head routers and experts
+    h = moe.moe_dims.make(64, 256, 8, 64, top_k=2, n_heads=2, head_dim=128)
+    with pytest.raises(ValueError, match="w_router"):
+        moe.moe_forward_headlocal(h, bf(64 * 256), bf(2 * 8 * 128 - 1), None, bf(2 * 8 * 128 * 128),
+                                  bf(2 * 8 * 128 * 64), bf(64 * 256), None, None, torch.zeros(1, dtype=torch.uint8))
