@@ -29,7 +29,8 @@ class HLDev:
         out = torch.empty((c.T, c.d), dtype=torch.bfloat16, device="cuda")
         idx = torch.empty((c.n_heads, c.T, c.top_k), dtype=torch.int32, device="cuda")
         logits = torch.empty((c.n_heads, c.T, c.E), dtype=torch.float32, device="cuda")
-        moe.moe_forward_headlocal(self.dims, self.x, self.w_router, None, self.w13, self.w_down, out, idx, logits,
+        bias = None if self.inp["bias"] is None else torch.from_numpy(np.ascontiguousarray(self.inp["bias"])).cuda()
+        moe.moe_forward_headlocal(self.dims, self.x, self.w_router, bias, self.w13, self.w_down, out, idx, logits,
                                   self.ws)
         return out, idx, logits
 
@@ -43,6 +44,8 @@ def _check(inp, out, idx, logits, tokens=None):
         idx_np, lg = idx_np[:, tokens], lg[:, tokens]
     for j in range(cfg.n_heads):
         s_ref = xw[:, j * cfg.head_dim:(j + 1) * cfg.head_dim] @ O.widen_bf16(inp["w_router"][j]).T
+        if inp["bias"] is not None:
+            s_ref = s_ref + np.asarray(inp["bias"][j], dtype=np.float64)[None, :]
         p = O.softmax(s_ref)
         gates = O.renormalised_gates(p, idx_np[j])
         G.check_routing(s_ref, idx_np[j], gates.astype(np.float32), cfg.top_k, lg[j])
@@ -76,3 +79,20 @@ def test_headlocal_workload_sampled():
     # deterministic
     out2, _, _ = dev.forward()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_headlocal_per_head_router_bias():
+    # a [n_heads, E] router bias moves each head's own selection and gates
+    inp = mi.make_inputs(mi.custom_config("hlb", head_local=True, T=500, d=512, n_heads=4, head_dim=128, E=32,
+                                          inter=64, top_k=4))
+    rng = np.random.default_rng(8)
+    inp["bias"] = rng.normal(0.0, 3.0, (4, 32)).astype(np.float32)
+    dev = HLDev(inp)
+    out, idx, logits = dev.forward()
+    assert moe.moe_get_device_status(dev.ws) == 0
+    _check(inp, out, idx, logits)
+    # the bias is the only difference from the unbiased layer, and it changes the routing
+    inp0 = dict(inp)
+    inp0["bias"] = None
+    _, idx0, _ = HLDev(inp0).forward()
+    assert not torch.equal(idx, idx0)
