@@ -85,6 +85,7 @@ _SIGS = {
     "moe_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_route_fused": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_route_two_stage": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_prepare_router": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "moe_route_folded": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_folded": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -260,6 +261,16 @@ def moe_route(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, str
     _dev(topk_idx, dtype=torch.int32)
     _check(lib().moe_route(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(topk_idx),
                            _ptr(topk_gate), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def moe_route_two_stage(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, topk_idx=topk_idx, topk_gate=topk_gate, logits=logits)
+    _dev(x, w_lat, w_head, dtype=torch.bfloat16)
+    _dev(bias, topk_gate, logits, dtype=torch.float32)
+    _dev(topk_idx, dtype=torch.int32)
+    _check(lib().moe_route_two_stage(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias),
+                                     _ptr(topk_idx), _ptr(topk_gate), _ptr(logits), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "moe_route_two_stage")
 
 
 def moe_route_fused(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, stream=None) -> None:

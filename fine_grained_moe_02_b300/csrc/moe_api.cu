@@ -77,6 +77,18 @@ T* at(void* ws, size_t off) {
 
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
 
+// Router choice of moe_route: small batches on chip (h stays in tensor
+// memory), the rest through the two-stage path.  With few 128-token tiles the
+// two-stage router's score GEMM has too few tiles to stream the latent back
+// at full bandwidth.  Measured on B300 (d = 4096, E = 128, 12 x 256 heads):
+// on chip 0.098 against 0.126 ms at 32 token tiles x 12 heads (T = 4096),
+// slower from 40 tiles (T = 5120); the bound is 3 waves of 148 SMs.
+constexpr int64_t kOnChipRouterItems = 3 * 148;
+
+bool route_on_chip(const moe_dims* d) {
+  return route_fused_supported(d->head_dim) && ((d->T + 127) / 128) * static_cast<int64_t>(d->n_heads) <= kOnChipRouterItems;
+}
+
 // moe_forward_host runs the layer over token chunks of ceil(T / n) tokens,
 // n = min(ceil(T / 8192), 8).  x comes in on one stream and out goes back on
 // another, so while chunk i computes on the caller's stream the copy engines
@@ -101,8 +113,19 @@ int64_t host_chunk_tokens(int64_t T) {
   return (T + n - 1) / n;
 }
 
+// A batch that moe_forward would route on chip runs as one piece (on-chip
+// routing of a smaller piece could sum the head scores in another order);
+// otherwise every piece takes the two-stage router, which gives each token
+// the bits it gets in the whole batch.
+bool host_one_piece(const moe_dims* d) { return route_on_chip(d); }
+
 // The pieces the layer runs over, in token order; returns their count.
-int host_pieces(int64_t T, int64_t* start, int64_t* len) {
+int host_pieces(int64_t T, int64_t* start, int64_t* len, bool one_piece) {
+  if (one_piece) {
+    start[0] = 0;
+    len[0] = T;
+    return 1;
+  }
   const int n = host_chunks(T);
   const int64_t tc = host_chunk_tokens(T);
   int m = 0;
@@ -172,7 +195,7 @@ bool host_pipe_ready(HostPipe& p) {
 // word collects the flags of every chunk.
 int forward_impl(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
                  const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws,
-                 size_t ws_bytes, void* stream, bool clear_status) {
+                 size_t ws_bytes, void* stream, bool clear_status, bool two_stage_router = false) {
   int rc = moe_check_dims(dims);
   if (rc != MOE_OK) return rc;
   if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
@@ -196,7 +219,10 @@ int forward_impl(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat,
   // cp.async gather warps, but on the clip workload it runs 9.8-9.9 ms
   // against 8.0-8.3 ms for GEMM-1 on x_perm plus ~1.05 ms for the gather.)
   moe_bf16* yperm = xperm;
-  if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  rc = two_stage_router
+           ? moe_route_two_stage(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)
+           : moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream);
+  if (rc != MOE_OK) return rc;
   if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, xperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_expert_gemm1(dims, xperm, offsets, w13, act, ws, ws_bytes, stream)) != MOE_OK) return rc;
   if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
@@ -257,7 +283,7 @@ int moe_workspace_size_host(const moe_dims* dims, size_t* bytes) {
   const int rc = moe_check_dims(dims);
   if (rc != MOE_OK) return rc;
   moe_dims chunk = *dims;
-  chunk.T = host_chunk_tokens(dims->T);
+  chunk.T = host_one_piece(dims) ? dims->T : host_chunk_tokens(dims->T);
   const size_t io = align_up(static_cast<size_t>(dims->T) * dims->d * 2, kAlign);
   *bytes = forward_layout(&chunk).end + 2 * io;
   return MOE_OK;
@@ -300,6 +326,16 @@ int moe_prepare_weights(const moe_dims* dims, const moe_bf16* w_gate, const moe_
 int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
               const float* bias, int32_t* topk_idx, float* topk_gate, float* logits, void* ws, size_t ws_bytes,
               void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (route_on_chip(dims))
+    return moe_route_fused(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, ws_bytes, stream);
+  return moe_route_two_stage(dims, x, w_lat, w_head, bias, topk_idx, topk_gate, logits, ws, ws_bytes, stream);
+}
+
+int moe_route_two_stage(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                        const float* bias, int32_t* topk_idx, float* topk_gate, float* logits, void* ws,
+                        size_t ws_bytes, void* stream) {
   int rc = moe_check_dims(dims);
   if (rc != MOE_OK) return rc;
   if (x == nullptr || w_lat == nullptr || w_head == nullptr || topk_idx == nullptr || topk_gate == nullptr ||
@@ -693,6 +729,10 @@ int moe_route_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x, c
   a.ext = route_ext_of(ext);
   a.status = status_ptr(ws);
   a.sm_count = sms;
+  if (route_on_chip(dims)) {  // the same choice as moe_route
+    a.partial = at<float>(ws, sl.hl);
+    return launch_route_fused(a, dims->head_dim, static_cast<cudaStream_t>(stream));
+  }
   return launch_route(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -742,9 +782,10 @@ int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf1
   size_t need = 0;
   if ((rc = moe_workspace_size_host(dims, &need)) != MOE_OK) return rc;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  const int64_t T = dims->T, tc = host_chunk_tokens(T);
+  const bool one_piece = host_one_piece(dims);
+  const int64_t T = dims->T, tc = one_piece ? T : host_chunk_tokens(T);
   int64_t p_start[kHostPiecesMax], p_len[kHostPiecesMax];
-  const int n = host_pieces(T, p_start, p_len);
+  const int n = host_pieces(T, p_start, p_len, one_piece);
   const size_t row = static_cast<size_t>(dims->d);  // elements per token
   moe_dims cd = *dims;
   cd.T = tc;
@@ -773,7 +814,8 @@ int moe_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf1
     cd.T = p_len[i];
     good = ok(cudaStreamWaitEvent(s, p.in_done[i], 0));
     if (good)
-      rc = forward_impl(&cd, x_dev + off, w_lat, w_head, bias, w13, w_down, out_dev + off, ws, inner, stream, false);
+      rc = forward_impl(&cd, x_dev + off, w_lat, w_head, bias, w13, w_down, out_dev + off, ws, inner, stream, false,
+                        /*two_stage_router=*/!one_piece);
     if (good && rc == MOE_OK)
       good = ok(cudaEventRecord(p.fwd_done[i], s)) && ok(cudaStreamWaitEvent(p.out, p.fwd_done[i], 0)) &&
              ok(cudaMemcpyAsync(out_host + off, out_dev + off, bytes, cudaMemcpyDeviceToHost, p.out));

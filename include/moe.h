@@ -142,10 +142,23 @@ int moe_prepare_weights(const moe_dims* dims, const moe_bf16* w_gate, const moe_
  *   ws       scratch of at least moe_scratch_size bytes
  * The latent vector h is accumulated in fp32 on the tensor cores and fed to
  * the head-score product as a bf16 hi + lo pair, so s carries fp32-level
- * accuracy although both products run as bf16 tensor-core GEMMs. */
+ * accuracy although both products run as bf16 tensor-core GEMMs.
+ * Small batches (ceil(T / 128) * n_heads <= 444, three waves of B300's 148
+ * SMs, and a head_dim moe_route_fused supports) take the on-chip path of
+ * moe_route_fused, where h never leaves the SM; larger ones take the
+ * two-stage path of moe_route_two_stage, which writes h to the workspace as
+ * the bf16 pair and is faster once there are enough token tiles.  Both meet
+ * the same tolerances; their last bits of s may differ. */
 int moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
               const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
               void* ws, size_t ws_bytes, void* stream);
+
+/* moe_route through the two-stage path at any size: a latent GEMM whose
+ * epilogue writes h as the bf16 hi | lo pair into the workspace, then a score
+ * GEMM over [h_hi | h_lo] with the softmax / top-k / gates in its epilogue. */
+int moe_route_two_stage(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                        const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
+                        void* ws, size_t ws_bytes, void* stream);
 
 /* moe_route with the latent vector kept on chip: one persistent tensor-core
  * kernel accumulates each head's 128-token x head_dim block of h in tensor
@@ -305,7 +318,8 @@ int moe_workspace_size_ext(const moe_dims* dims, const moe_ext* ext, size_t* byt
 /* Routing with modality ranges; writes top_k + n_shared slots per token
  * (topk_idx/topk_gate [T, top_k + n_shared]: the routed slots, then the
  * shared experts with gate 1).  logits [T, E] (optional) are the unmasked
- * summed scores.  Other arguments as in moe_route. */
+ * summed scores.  Other arguments, and the choice between the on-chip and
+ * the two-stage path, as in moe_route. */
 int moe_route_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x, const moe_bf16* w_lat,
                   const moe_bf16* w_head, const float* bias, int32_t* topk_idx, float* topk_gate, float* logits,
                   void* ws, size_t ws_bytes, void* stream);
@@ -349,8 +363,10 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
  * n >= 3 the first and last chunk are cut 1:3, the short piece at the end of
  * the batch): the chunks' copies to the device run on one internal stream
  * and the copies back on another, overlapping the compute of the
- * neighbouring chunks on `stream`.  Each token's result has the same bits as moe_forward over the
- * whole batch.  The device status word at the start of ws collects the flags
+ * neighbouring chunks on `stream`.  A batch that moe_route would route on
+ * chip runs as one piece; otherwise every piece takes the two-stage router.
+ * Each token's result has the same bits as moe_forward over the whole
+ * batch.  The device status word at the start of ws collects the flags
  * of every chunk.  Host buffers should be page-locked: pageable memory still
  * gives correct results, but the copies then serialise with the compute.
  * Calls for the same device are serialised by an internal lock.  ws: at

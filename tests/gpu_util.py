@@ -77,6 +77,14 @@ class Dev:
         moe.moe_route(self.dims, self.x, self.w_lat, self.w_head, self.bias, idx, gate, logits, self.ws)
         return idx, gate, logits
 
+    def route_two_stage(self):
+        T, k, E = self.cfg.T, self.cfg.top_k, self.cfg.E
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        moe.moe_route_two_stage(self.dims, self.x, self.w_lat, self.w_head, self.bias, idx, gate, logits, self.ws)
+        return idx, gate, logits
+
     def route_fused(self):
         T, k, E = self.cfg.T, self.cfg.top_k, self.cfg.E
         idx = torch.empty((T, k), dtype=torch.int32, device="cuda")

@@ -23,13 +23,16 @@ pytestmark = pytest.mark.gpu
     dict(T=140, d=256, E=24, inter=64, n_heads=1, head_dim=512),       # two-stage only
     dict(T=1000, d=1024, E=128, inter=64),                              # on-chip: several head groups
 ])
-@pytest.mark.parametrize("path", ["two_stage", "fused"])
+@pytest.mark.parametrize("path", ["auto", "two_stage", "fused"])
 def test_router_matches_oracle(kw, path):
+    # auto = moe_route, which picks the on-chip path for small batches
     inp = G.small_inputs(**kw)
     cfg = inp["cfg"]
     dev = G.Dev(inp)
-    if path == "two_stage":
+    if path == "auto":
         idx, gate, logits = dev.route()
+    elif path == "two_stage":
+        idx, gate, logits = dev.route_two_stage()
     else:
         if cfg.head_dim % 64 or cfg.head_dim > 256:
             pytest.skip("the on-chip router covers head_dim % 64 == 0, <= 256")
@@ -84,7 +87,7 @@ def test_exact_ties_go_to_the_lower_index(path):
     inp["bias"] = np.ascontiguousarray(gb[np.arange(E) % ng])
     dev = G.Dev(inp)
     if path == "two_stage":
-        idx, gate, logits = dev.route()
+        idx, gate, logits = dev.route_two_stage()
     elif path == "fused":
         idx, gate, logits = dev.route_fused()
     else:

@@ -78,12 +78,14 @@ def test_forward_host_buffers():
     assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
 
 
-@pytest.mark.parametrize("T,pinned", [(8193, True), (20000, True), (9000, False)])
-def test_forward_host_chunks_match_one_forward(T, pinned):
+@pytest.mark.parametrize("T,pinned,heads", [(8193, True, 12), (20000, True, 12), (9000, False, 12), (20000, True, 1)])
+def test_forward_host_chunks_match_one_forward(T, pinned, heads):
     # 2 or 3 token chunks with a ragged last one, copies overlapping compute
     # (pinned) or serialised with it (pageable): the same bits as one
-    # moe_forward over the whole batch, and the oracle on tokens of every chunk
-    inp = G.small_inputs(T=T, d=512, E=32, inter=128, seed=3)
+    # moe_forward over the whole batch, and the oracle on tokens of every
+    # chunk.  With one 256-dim head the whole batch routes on chip, so it
+    # runs as one piece.
+    inp = G.small_inputs(T=T, d=512, E=32, inter=128, seed=3, n_heads=heads, head_dim=256)
     dev = G.Dev(inp)
     ref = dev.forward()
     idx, _, _ = dev.route(want_logits=False)
