@@ -1,6 +1,7 @@
 // Gate-weighted combine: out[t] = sum_s gate[t,s] * y_perm[row_of[t,s]].
-// One warp per token, scatter-free (each output row has one writer), fp32
-// accumulation in slot order, one bf16 rounding.  16-byte vector loads.
+// One warp per (head, token) unit, grid-stride, scatter-free (each output row
+// has one writer), fp32 accumulation in slot order, one bf16 rounding.
+// 16-byte vector loads.
 // Follows the last step of the MagiMoE operator library's routing -> sorting ->
 // calculation chain ("Sand.ai: The world's first 100-billion-parameter open-source MoE video generation model MAGI Preview" (36kr), section "02. Two Key Technical Decision Points"):
 // the routed experts' outputs are brought back to token order and summed.
@@ -32,21 +33,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   const int64_t wg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const uint4* y0 = y;
+  uint4* out0 = out;
   const int32_t* row_of0 = row_of;
   const float* gate0 = gate;
-  uint4* out0 = out;
-  for (int64_t ht = wg; ht < T * heads; ht += nw) {
-    const int64_t h = ht / T, t = ht - h * T;  // (head, token): head h's outputs go to its d columns
+  const int64_t units = T * heads;
+  // (head, token) unit ht: head h's outputs go to its d columns.  The next
+  // unit's rows and gates are loaded while this one is summed (with short
+  // rows, e.g. one 512-byte head slice per lane group, that load chain would
+  // otherwise be exposed on every unit).
+  int r_n = -1;
+  float g_n = 0.f;
+  if (wg < units && lane < k) {
+    const int64_t h = wg / T, t = wg - h * T;
+    r_n = __ldg(row_of0 + h * T * k + t * k + lane);
+    g_n = __ldg(gate0 + h * T * k + t * k + lane);
+  }
+  for (int64_t ht = wg; ht < units; ht += nw) {
+    const int64_t h = ht / T, t = ht - h * T;
     y = y0 + h * rows * d_vec;
-    row_of = row_of0 + h * T * k;
-    gate = gate0 + h * T * k;
     out = out0 + h * d_vec;
-    int r_l = -1;
-    float g_l = 0.f;
-    if (lane < k) {
-      r_l = __ldg(row_of + t * k + lane);
-      g_l = __ldg(gate + t * k + lane);
-      if (r_l < 0 || r_l >= rows) r_l = -1;
+    int r_l = r_n;
+    const float g_l = g_n;
+    if (lane < k && (r_l < 0 || r_l >= rows)) r_l = -1;
+    const int64_t nx = ht + nw;
+    if (nx < units && lane < k) {
+      const int64_t h2 = nx / T, t2 = nx - h2 * T;
+      r_n = __ldg(row_of0 + h2 * T * k + t2 * k + lane);
+      g_n = __ldg(gate0 + h2 * T * k + t2 * k + lane);
     }
     int r[KMAX];
     float g[KMAX];
