@@ -323,28 +323,123 @@ __device__ __forceinline__ void topk_insert(float (&bv)[kMaxTopK], int (&bi)[kMa
   }
 }
 
+// Columns [col, col + 32) of the row's score accumulator (only the first 16
+// when !two), bias added; the missing half reads as -inf.
+__device__ __forceinline__ void topk_load(const TopKParams& p, uint32_t taddr, int col, bool two, float (&s)[32]) {
+  uint32_t u[32];
+  __syncwarp();
+  ptx::tmem_ld16(taddr + col, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+  if (two) ptx::tmem_ld16(taddr + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
+  ptx::tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    s[j] = (j < 16 || two) ? __uint_as_float(u[j]) : -INFINITY;
+    if (p.bias != nullptr && (j < 16 || two) && col + j < p.E) s[j] += __ldg(p.bias + col + j);
+  }
+}
+
+// v[j] for a j that differs between lanes, from registers: a 5-level select
+// tree on the bits of j (a dynamic register index would go through local
+// memory).
+__device__ __forceinline__ float topk_pick(const float (&v)[32], int j) {
+  float a[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = (j & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = (j & 2) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = (j & 4) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) a[i] = (j & 8) ? a[2 * i + 1] : a[2 * i];
+  return (j & 16) ? a[1] : a[0];
+}
+
 // Scans the row's columns [c0, c1) (multiples of 16) of the score
 // accumulator: bias, optional logits output, and the running top list for
 // experts in [e_lo, e_hi).
+//
+// Each thread owns one row, and with k winners in every row nearly every
+// column holds a winner of some lane of the warp, so inserting column by
+// column makes the whole warp run an insertion at almost every column.  The
+// scan therefore runs twice.  The first pass takes the maximum of each of
+// kTauGroups column groups (column j of a 32-column batch is in group
+// j % kTauGroups) and sets tau to the k-th largest of those maxima: k
+// different groups hold a score >= tau, so the k-th best score of the range
+// is >= tau and no member of the top k (ties included) is below it.  The
+// second pass marks each lane's columns with s >= tau, a few per batch, and
+// inserts only those, in column order, one per lane per step: the list then
+// ends with the same first k entries as a scan of every column would.  Only
+// the first k entries are used (written out or merged); later slots may
+// differ from a full scan's.  NaN scores are never inserted, as before.
 __device__ __forceinline__ void topk_scan(const TopKParams& p, uint32_t taddr, int c0, int c1, int e_lo, int e_hi,
                                           float* lrow, float (&bv)[kMaxTopK], int (&bi)[kMaxTopK]) {
+  constexpr int kTauGroups = 16;
+  static_assert(kTauGroups >= kMaxTopK, "tau needs at least k groups");
+  if (e_hi > p.E) e_hi = p.E;
+  float gm[kTauGroups];
+#pragma unroll
+  for (int g = 0; g < kTauGroups; ++g) gm[g] = -INFINITY;
 #pragma unroll 1
   for (int col = c0; col < c1; col += 32) {
-    uint32_t u[32];
     const bool two = col + 16 < c1;
-    __syncwarp();
-    ptx::tmem_ld16(taddr + col, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
-    if (two) ptx::tmem_ld16(taddr + col + 16, *reinterpret_cast<uint32_t(*)[16]>(&u[16]));
-    ptx::tmem_ld_wait();
+    float s[32];
+    topk_load(p, taddr, col, two, s);
+    const int lo = e_lo - col, hi = e_hi - col;
+    if (__all_sync(0xffffffffu, lo <= 0 && hi >= (two ? 32 : 16))) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = col + j;
-      if ((j < 16 || two) && e < p.E) {
-        float s = __uint_as_float(u[j]);
-        if (p.bias != nullptr) s += __ldg(p.bias + e);
-        if (lrow != nullptr) lrow[e] = s;
-        if (e >= e_lo && e < e_hi && s > bv[kMaxTopK - 1]) topk_insert(bv, bi, s, e);
+      for (int j = 0; j < 32; ++j) gm[j % kTauGroups] = fmaxf(gm[j % kTauGroups], s[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j >= lo && j < hi) gm[j % kTauGroups] = fmaxf(gm[j % kTauGroups], s[j]);
+    }
+    if (lrow != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if ((j < 16 || two) && col + j < p.E) lrow[col + j] = s[j];
+    }
+  }
+  // descending bitonic sort of the group maxima; tau = the k-th largest
+  constexpr int kLog = 4;
+  static_assert(kTauGroups == 1 << kLog, "bitonic network size");
+#pragma unroll
+  for (int lg = 1; lg <= kLog; ++lg) {  // merged run length 2^lg
+#pragma unroll
+    for (int ls = kLog - 1; ls >= 0; --ls) {  // compare distance 2^ls, for ls < lg
+#pragma unroll
+      for (int i = 0; i < kTauGroups; ++i) {
+        const int l = i ^ (1 << ls);
+        if (ls < lg && l > i) {
+          const float x = gm[i], y = gm[l];
+          const bool desc = (i & (1 << lg)) == 0;
+          gm[i] = desc ? fmaxf(x, y) : fminf(x, y);
+          gm[l] = desc ? fminf(x, y) : fmaxf(x, y);
+        }
       }
+    }
+  }
+  // a select chain, not gm[p.k - 1]: an indexed read would put gm in local memory
+  float tau = gm[kMaxTopK - 1];
+#pragma unroll
+  for (int q = kMaxTopK - 2; q >= 0; --q) tau = (p.k - 1 <= q) ? gm[q] : tau;
+#pragma unroll 1
+  for (int col = c0; col < c1; col += 32) {
+    const bool two = col + 16 < c1;
+    float s[32];
+    topk_load(p, taddr, col, two, s);
+    const int lo = e_lo - col, hi = e_hi - col;
+    uint32_t mask = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j >= lo && j < hi && s[j] >= tau) mask |= 1u << j;
+    const int steps = __reduce_max_sync(0xffffffffu, __popc(mask));
+#pragma unroll 1
+    for (int it = 0; it < steps; ++it) {
+      const int j = __ffs(mask) - 1;  // -1 once this lane has no candidate left
+      mask &= mask - 1;
+      const float v = topk_pick(s, j & 31);
+      // -inf leaves the list unchanged: every entry is >= it
+      topk_insert(bv, bi, (j >= 0 && v > bv[kMaxTopK - 1]) ? v : -INFINITY, col + j);
     }
   }
 }
