@@ -347,8 +347,9 @@ int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x,
  *   logits [n_heads, T, E] fp32 or NULL (written: each head's scores)
  * Rules: head_dim % 64 == 0, inter % 64 == 0, E <= 256, top_k <= min(8, E).
  * All heads' routers run as one batched GEMM, their sorts, gathers and
- * combines as single launches over (head, token); the expert GEMMs run head
- * by head on `stream`, each head in its own slice of the workspace. */
+ * combines as single launches over (head, token), each expert layer as one
+ * grouped GEMM over all n_heads * E experts (head by head when
+ * n_heads * E > 3072), all on `stream`. */
 int moe_workspace_size_headlocal(const moe_dims* dims, size_t* bytes);
 int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
                                   void* stream);
