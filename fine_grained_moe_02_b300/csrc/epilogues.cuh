@@ -429,11 +429,19 @@ __device__ __forceinline__ void topk_scan(const TopKParams& p, uint32_t taddr, i
     topk_load(p, taddr, col, two, s);
     const int lo = e_lo - col, hi = e_hi - col;
     uint32_t mask = 0;
+    if (__all_sync(0xffffffffu, lo <= 0 && hi >= (two ? 32 : 16))) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j >= lo && j < hi && s[j] >= tau) mask |= 1u << j;
+      for (int j = 0; j < 32; ++j)
+        if (s[j] >= tau) mask |= 1u << j;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j >= lo && j < hi && s[j] >= tau) mask |= 1u << j;
+    }
     const int steps = __reduce_max_sync(0xffffffffu, __popc(mask));
-#pragma unroll 1
+    // unrolled by two: the next candidate's lookup does not depend on the
+    // list and overlaps the current insertion
+#pragma unroll 2
     for (int it = 0; it < steps; ++it) {
       const int j = __ffs(mask) - 1;  // -1 once this lane has no candidate left
       mask &= mask - 1;
