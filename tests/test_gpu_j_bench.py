@@ -33,3 +33,11 @@ def test_bench_prints_one_contract_line():
     e = j["e2e"]
     assert e["unit"] == "tokens/s" and e["value"] > 0
     assert e["h2d_bytes_per_step"] == e["d2h_bytes_per_step"] == 256 * 512 * 2
+
+
+def test_graft_entry_smoke_runs_the_layer_on_cuda0():
+    # the entry point's smoke(): one tiny forward through libmoe checked against the oracle
+    r = subprocess.run([sys.executable, "-c", "import __graft_entry__ as g; g.smoke()"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "smoke ok" in r.stdout
