@@ -18,7 +18,7 @@
 namespace moe {
 
 constexpr int kTokBlock = 2048;   // tokens per hist/assign block
-constexpr int kAssignWarps = 8;   // warps per assign block; each owns kTokBlock/8 tokens
+constexpr int kAssignWarps = 16;  // warps per assign block; each owns kTokBlock/16 tokens
 
 // Loads token t's k expert ids.  An id outside [0, E), or a repeat of an
 // earlier slot's id, becomes -1 (left out of the permutation) and sets *bad.
