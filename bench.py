@@ -229,16 +229,31 @@ def cpu_baseline(inp, n_tokens: int) -> dict:
                       f"forward incl. per-expert bf16->fp64 widening ({dt:.1f} s)"}
 
 
+def host_available_bytes() -> int:
+    """Host memory available to this process, from /proc/meminfo (MemAvailable),
+    else free pages from sysconf; 0 if neither can be read (the oracle then
+    widens the weights per step instead of once)."""
+    try:
+        for line in Path("/proc/meminfo").read_text().splitlines():
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    try:
+        return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 0
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    import psutil
     from oracle import moe_oracle as O
     cfg = mi.CONFIGS[args.workload]
     inp = mi.make_inputs(cfg)
     weight_bytes_f64 = 8 * (inp["w_gate"].size + inp["w_up"].size + inp["w_down"].size)
     widened = None
-    if psutil.virtual_memory().available > 2.5 * weight_bytes_f64:
+    if host_available_bytes() > 2.5 * weight_bytes_f64:
         widened = {k: O.widen_bf16(inp[k]) for k in ("w_lat", "w_head", "w_gate", "w_up", "w_down")}
     per_step = max(16, min(256, 4096 // max(1, args.steps + args.warmup)))
     for i in range(args.warmup):

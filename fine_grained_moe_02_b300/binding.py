@@ -333,8 +333,9 @@ def moe_expert_gemm1_gather(dims, x, src_token, offsets, w13, act, ws, stream=No
 
 
 def moe_dispatch_noalloc(dims, x, topk_idx, offsets, row_of, src_token, x_perm, status=None, stream=None) -> None:
-    _need(dims, x=x, topk_idx=topk_idx, offsets=offsets, row_of=row_of, src_token=src_token, x_perm=x_perm, status=status)
     """moe_dispatch without a workspace (scratch in a fixed array inside libmoe)."""
+    _need(dims, x=x, topk_idx=topk_idx, offsets=offsets, row_of=row_of, src_token=src_token, x_perm=x_perm,
+          status=status)
     _dev(x, x_perm, dtype=torch.bfloat16)
     _dev(topk_idx, offsets, row_of, src_token, status, dtype=torch.int32)
     _check(lib().moe_dispatch_noalloc(ctypes.byref(dims), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(row_of),

@@ -5,7 +5,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "internal.h"
 #include "moe.h"
@@ -19,23 +18,17 @@ constexpr int64_t kSinkInts = 64;  // status sink when the caller passes no stat
 // Lives for as long as the library is loaded, on every GPU that loads it.
 static __device__ __align__(256) int32_t g_dispatch_scratch[kSinkInts + 2 * kNoAllocMaxCells];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int32_t* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_dispatch_scratch on the current device.  Host code may
+// Device address of g_dispatch_scratch in the current context.  Host code may
 // not use the symbol itself (on the host it names a stand-in, not device
-// memory), so the address is looked up once per device and cached.
+// memory).  The address is looked up on every call rather than cached per
+// device: a cudaDeviceReset, or another context on the same device, loads
+// the module again at a different address, and a cached pointer would then
+// aim at memory that is no longer this array.  The lookup allocates nothing;
+// the first one in a context loads the module there.
 int scratch_address(int32_t** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+  *out = static_cast<int32_t*>(p);
   return MOE_OK;
 }
 

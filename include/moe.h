@@ -236,9 +236,11 @@ int moe_dispatch_indices(const moe_dims* dims, const int32_t* topk_idx, int32_t*
  *     the caller clears it).  NULL: device-detected problems are not reported.
  *   - Limit: ceil(T / 2048) * E <= 65536 (e.g. T <= 1,048,576 at E = 128);
  *     larger problems return MOE_ERR_UNSUPPORTED_SHAPE and launch nothing.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - Every call looks up the array's address in the current context
+ *     (cudaGetSymbolAddress, which allocates nothing), so the entry point
+ *     stays correct after a cudaDeviceReset or under another context on the
+ *     same device.  The first call in a context also loads the library's
+ *     device code there: make that first call before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents.  Every counter is rewritten before it is read, so nothing
  *     needs clearing, but calls that overlap on the GPU (different streams,

@@ -24,3 +24,14 @@ def test_reference_arm_prints_one_contract_line():
     assert j["cpu_baseline"]["value"] == j["value"]
     assert j["e2e"] == {"value": j["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert j["config"]["workload"].startswith("clip: T=107520")
+
+
+def test_reference_arm_needs_no_psutil():
+    # the GPU image has no psutil: the arm must size host memory without it
+    code = ("import sys, runpy; sys.modules['psutil'] = None; "
+            "sys.argv = ['bench.py', '--impl', 'reference', '--steps', '1', '--warmup', '1']; "
+            "runpy.run_path('bench.py', run_name='__main__')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1 and json.loads(lines[0])["impl"] == "reference"
