@@ -39,6 +39,8 @@ import moe_inputs as mi  # noqa: E402
 METRIC = "MoE-layer tokens/sec on 1 B300; grouped-GEMM % bf16 TC peak; permute GB/s"
 KERNELS_PER_STEP = 9  # 2 router GEMMs, 4 sorting kernels, 2 expert GEMMs, combine
 GEMM_SOURCES = ["gemm_tc.cuh", "epilogues.cuh", "ptx.cuh", "gemm_launch.cu"]
+NOMINAL_BF16_TFLOPS = 2250.0   # B300 dense bf16 at its maximum SM clock
+NOMINAL_SM_MHZ = 2032.0
 
 
 def parse():
@@ -316,11 +318,17 @@ def measure_headlocal_variant(torch, moe, steps: int) -> dict:
                  + H * E * (2 * I * Dh + Dh * I) * 2          # expert weights
                  + 2 * H * Tk * Dh * 2 + 2 * H * Tk * I * 2   # x_perm, act: written and read
                  + 2 * H * Tk * Dh * 2 + T * cfg.d * 2)       # y_perm written and read, out
+    # the method's own bytes: x read once, router and expert weights, out written
+    essential = T * cfg.d * 2 + H * E * Dh * 2 + H * E * (2 * I * Dh + Dh * I) * 2 + T * cfg.d * 2
     hbm = peaks()["hbm"]
     return {"workload": cfg.note, "value": cfg.T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "layer_tflops": flops / (ms * 1e-3) / 1e12,
-            "algorithmic_bytes": alg_bytes, "hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
-            "frac_hbm": alg_bytes / (ms * 1e-3) / 1e9 / hbm,
+            "essential_bytes": essential, "essential_gbs": essential / (ms * 1e-3) / 1e9,
+            "frac_hbm": essential / (ms * 1e-3) / 1e9 / hbm,
+            "frac_hbm_note": "essential bytes (x, router and expert weights, out) over the layer time",
+            "traffic_bytes": alg_bytes, "traffic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+            "traffic_frac": alg_bytes / (ms * 1e-3) / 1e9 / hbm,
+            "traffic_note": "bytes of this implementation incl. its x_perm, act and y_perm round trips",
             "path": "moe_forward_headlocal: all heads' routers + top-k as one batched GEMM, one sort and gather "
                     "over (head, token), grouped SwiGLU GEMMs head by head, one combine into each head's columns"}
 
@@ -511,6 +519,54 @@ def main():
     if moe.moe_get_device_status(ws) != 0:
         raise SystemExit("device status set by a router variant")
 
+    # moe_forward_fused: the gather inside expert GEMM-1, the gate inside expert
+    # GEMM-2's epilogue, and both, timed in rounds that interleave them with the
+    # plain moe_forward (one call each per round), so clock drift under the
+    # power cap does not favour whichever ran first
+    calls = {"plain": 0, "gather_in_gemm1": 1, "gate_in_gemm2": 2, "gather_and_gate": 3}
+    for fuse in calls.values():
+        moe.moe_forward_fused(dims, x, w_lat, w_head, bias, w13, w_down, out, fuse, ws)
+    evs_f = {n: [] for n in calls}
+    barrier()
+    for _ in range(max(3, args.steps // 4)):
+        for name, fuse in calls.items():
+            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            e[0].record(stream)
+            moe.moe_forward_fused(dims, x, w_lat, w_head, bias, w13, w_down, out, fuse, ws)
+            e[1].record(stream)
+            evs_f[name].append(e)
+    barrier()
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status set by moe_forward_fused")
+    fused = {}
+    for name in calls:
+        f_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs_f[name]), world, "cuda")
+        fused[name] = {"value": throughput(T, world, 1, f_ms / 1e3), "unit": "tokens/s", "ms_per_step": f_ms}
+    # the gate fold stage by stage: expert GEMM-2 + combine against the gated
+    # GEMM-2 + row combine, alternating, on the routing of the last step
+    moe.moe_route(dims, x, w_lat, w_head, bias, idx, gate, None, ws)
+    moe.moe_dispatch(dims, x, idx, offsets, row_of, src, x_perm, ws)
+    moe.moe_expert_gemm1(dims, x_perm, offsets, w13, act, ws)
+    pair = {"plain": [], "gated": []}
+    for i in range(2 * max(3, args.steps // 5)):
+        kind = "plain" if i % 2 == 0 else "gated"
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        if kind == "plain":
+            moe.moe_expert_gemm2(dims, act, offsets, w_down, y_perm, ws)
+            ev[1].record(stream)
+            moe.moe_combine(dims, y_perm, row_of, gate, out)
+        else:
+            moe.moe_expert_gemm2_gated(dims, act, offsets, w_down, src, row_of, gate, y_perm, ws)
+            ev[1].record(stream)
+            moe.moe_combine_rows(dims, y_perm, row_of, out)
+        ev[2].record(stream)
+        pair[kind].append(ev)
+    barrier()
+    gate_fold = {k: {"gemm2_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in v),
+                     "combine_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in v)} for k, v in pair.items()}
+    fused["gate_fold_stages"] = gate_fold
+
     ext_variant = measure_ext_variant(torch, moe, max(3, args.steps // 2)) if cfg.name == "clip" else None
     hl_variant = measure_headlocal_variant(torch, moe, max(3, args.steps // 2)) if cfg.name == "clip" else None
 
@@ -572,13 +628,18 @@ def main():
                      "achieved": g1_tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": g1_tf / pk["bf16_sus"],
                      "peak_kind": f"bf16 dense sustained ({tag}; kernel timed inside a long step)",
                      "traffic": traffic, "traffic_note": traffic_note,
-                     "algorithmic_flops_per_launch": alg["gemm1_flops"]},
+                     "algorithmic_flops_per_launch": alg["gemm1_flops"],
+                     "frac_burst": g1_tf / pk["bf16"],
+                     "tflops_per_sm_mhz": g1_tf / clk["sm_mhz"] if clk.get("sm_mhz") else None,
+                     "frac_nominal_at_sampled_clock": (g1_tf / (NOMINAL_BF16_TFLOPS * clk["sm_mhz"] / NOMINAL_SM_MHZ)
+                                                       if clk.get("sm_mhz") else None)},
         "variants": {"folded_router": {
             "value": throughput(T, world, 1, fold_ms / 1e3), "unit": "tokens/s", "ms_per_step": fold_ms,
             "route_ms": fold_route_ms,
             "router_tflops": 2 * T * (2 * d) * E / (fold_route_ms * 1e-3) / 1e12,
             "path": "moe_forward_folded: router folded to s = x (W_head W_lat)^T + b, one bf16 hi/lo GEMM "
                     "(same outputs and tolerances; h never formed)"},
+            "fused_forward": fused,
             "modality_shared_experts": ext_variant,
             "head_local_moe": hl_variant,
             "on_chip_router": {
@@ -587,6 +648,8 @@ def main():
                 "path": "moe_route_fused: latent h kept in tensor memory, head-group partial scores only; "
                         "timed on its own (the step uses moe_route)"}},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches_note": "launches of libmoe kernels inside the timed step loop (route 2, sort 4, expert GEMMs 2, "
+                             "combine 1 per step)",
         "clocks": clk,
         "e2e": e2e,
     }

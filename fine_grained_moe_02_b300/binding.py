@@ -30,6 +30,8 @@ MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_TIMEOUT = 0x2
 MOE_DEV_BAD_OFFSETS = 0x4
 MOE_DEV_BAD_MODALITY = 0x8
+MOE_FUSE_GATHER = 0x1
+MOE_FUSE_GATE = 0x2
 
 
 class MoeError(RuntimeError):
@@ -97,6 +99,10 @@ _SIGS = {
     "moe_expert_gemm1": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_expert_gemm2": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P]),
+    "moe_expert_gemm2_gated": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_combine_rows": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
+    "moe_forward_fused": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_uint32, _P, ctypes.c_size_t,
+                                         _P]),
     "moe_forward": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_workspace_size_ext": (ctypes.c_int, [_DP, _XP, ctypes.POINTER(ctypes.c_size_t)]),
     "moe_route_ext": (ctypes.c_int, [_DP, _XP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -374,6 +380,35 @@ def moe_combine(dims, y_perm, row_of, topk_gate, out, stream=None) -> None:
     _dev(topk_gate, dtype=torch.float32)
     _check(lib().moe_combine(ctypes.byref(dims), _ptr(y_perm), _ptr(row_of), _ptr(topk_gate), _ptr(out),
                              _stream(stream)), "moe_combine")
+
+
+def moe_expert_gemm2_gated(dims, act, offsets, w_down, src_token, row_of, topk_gate, y_perm, ws,
+                           stream=None) -> None:
+    _need(dims, act=act, offsets=offsets, w_down=w_down, src_token=src_token, row_of=row_of, topk_gate=topk_gate,
+          y_perm=y_perm)
+    _dev(act, w_down, y_perm, dtype=torch.bfloat16)
+    _dev(offsets, src_token, row_of, dtype=torch.int32)
+    _dev(topk_gate, dtype=torch.float32)
+    _check(lib().moe_expert_gemm2_gated(ctypes.byref(dims), _ptr(act), _ptr(offsets), _ptr(w_down),
+                                        _ptr(src_token), _ptr(row_of), _ptr(topk_gate), _ptr(y_perm), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "moe_expert_gemm2_gated")
+
+
+def moe_combine_rows(dims, y_perm, row_of, out, stream=None) -> None:
+    _need(dims, y_perm=y_perm, row_of=row_of, out=out)
+    _dev(y_perm, out, dtype=torch.bfloat16)
+    _dev(row_of, dtype=torch.int32)
+    _check(lib().moe_combine_rows(ctypes.byref(dims), _ptr(y_perm), _ptr(row_of), _ptr(out), _stream(stream)),
+           "moe_combine_rows")
+
+
+def moe_forward_fused(dims, x, w_lat, w_head, bias, w13, w_down, out, fuse, ws, stream=None) -> None:
+    _need(dims, x=x, w_lat=w_lat, w_head=w_head, bias=bias, w13=w13, w_down=w_down, out=out)
+    _dev(x, w_lat, w_head, w13, w_down, out, dtype=torch.bfloat16)
+    _dev(bias, dtype=torch.float32)
+    _check(lib().moe_forward_fused(ctypes.byref(dims), _ptr(x), _ptr(w_lat), _ptr(w_head), _ptr(bias), _ptr(w13),
+                                   _ptr(w_down), _ptr(out), int(fuse), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_forward_fused")
 
 
 def moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws, stream=None) -> None:

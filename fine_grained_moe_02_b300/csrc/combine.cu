@@ -1,4 +1,5 @@
-// Gate-weighted combine: out[t] = sum_s gate[t,s] * y_perm[row_of[t,s]].
+// Gate-weighted combine: out[t] = sum_s gate[t,s] * y_perm[row_of[t,s]]
+// (gate == nullptr: the rows already carry their gates, weight 1 each).
 // One warp per (head, token) unit, grid-stride, scatter-free (each output row
 // has one writer), fp32 accumulation in slot order, one bf16 rounding.
 // 16-byte vector loads.
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   if (wg < units && lane < k) {
     const int64_t h = wg / T, t = wg - h * T;
     r_n = __ldg(row_of0 + h * T * k + t * k + lane);
-    g_n = __ldg(gate0 + h * T * k + t * k + lane);
+    g_n = gate0 != nullptr ? __ldg(gate0 + h * T * k + t * k + lane) : 1.0f;
   }
   for (int64_t ht = wg; ht < units; ht += nw) {
     const int64_t h = ht / T, t = ht - h * T;
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     if (nx < units && lane < k) {
       const int64_t h2 = nx / T, t2 = nx - h2 * T;
       r_n = __ldg(row_of0 + h2 * T * k + t2 * k + lane);
-      g_n = __ldg(gate0 + h2 * T * k + t2 * k + lane);
+      g_n = gate0 != nullptr ? __ldg(gate0 + h2 * T * k + t2 * k + lane) : 1.0f;
     }
     int r[KMAX];
     float g[KMAX];

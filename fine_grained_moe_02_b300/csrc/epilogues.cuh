@@ -75,18 +75,22 @@ __device__ __forceinline__ void release_accumulator(EpiCtx& ctx) {
   ctx.released = true;
 }
 
-// silu(g) = g * sigmoid(g) = h + h * tanh(h) with h = g / 2, since
-// sigmoid(g) = (1 + tanh(g / 2)) / 2.  One special-function op per value
-// (tanh.approx.f32, relative error about 2^-11) instead of two (exp and a
-// reciprocal): with few k-slices per tile the SwiGLU epilogue is bound by
-// that unit.  The error is about |g| * 2^-12: for g >= 0 at most ~2.4e-4
-// relative, below the bf16 rounding of act; for g < -10, where |silu(g)| <
-// 4.6e-4, the result is 0, so the absolute error stays below ~2.5e-3.
+// silu(g) = g * sigmoid(g) = g / (1 + e^-g): one ex2.approx for e^-g and one
+// rcp.approx for the reciprocal (relative errors about 2^-22 and 1 ulp), so
+// silu keeps fp32-level relative accuracy over the whole range, the negative
+// side included, where the form h + h tanh(h) (h = g / 2) loses it: there
+// 1 + tanh(h) cancels and tanh.approx's absolute error of ~2^-11 becomes a
+// large relative one.  Two special-function ops and three other ops per
+// value; a Newton-Raphson division in FMAs instead of the rcp (one
+// special-function op, nine others) measured slower in the short-K SwiGLU
+// epilogue of the head-local layer, which is bound by instruction issue.
+// Far below -88, e^-g overflows to inf and the result is -0 (true value
+// below 1e-36 in magnitude).
 __device__ __forceinline__ float silu(float g) {
-  const float h = 0.5f * g;
-  float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
-  return g < -10.0f ? 0.0f : fmaf(h, t, h);
+  float z, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(z) : "f"(-1.4426950408889634f * g));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + z));
+  return g * r;
 }
 
 __device__ __forceinline__ int warp_valid_rows(const TileCoord& c, const EpiCtx& ctx) {
@@ -119,6 +123,58 @@ struct EpiStoreBf16 {
       tmem_ld32(taddr + col, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) pk[col / 2 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    }
+    release_accumulator(ctx);
+    if (nvalid > 0) {
+#pragma unroll
+      for (int col = 0; col < BN; col += 64)
+        store_rows64(ctx, c.row0 + ctx.quad * 32, c.n_blk * BN + col, nvalid, pk + col / 2, row_ptr + col);
+    }
+  }
+};
+
+// Expert GEMM-2 with the gate multiply folded in:
+//   y_perm[r] = bf16(gate[t, s] * acc),  t = src_token[r], row_of[t, s] = r,
+// so the combine only sums a token's k rows.  Each thread finds its row's
+// gate before it reads the accumulator (src_token, then the k row_of / gate
+// entries of that token: L2-resident, their latency hidden behind the
+// accumulator loads).  A row outside the group, or whose token does not list
+// it, gets gate 0.
+struct EpiStoreGated {
+  static constexpr int kWarps = 4;
+  struct Params {
+    uint16_t* out;
+    int64_t ld;
+    const int32_t* src_token;  // [rows]
+    const int32_t* row_of;     // [T, k]
+    const float* gate;         // [T, k]
+    int64_t T;
+    int k;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const TileCoord& c, uint32_t taddr, int r,
+                                             EpiCtx& ctx) {
+    const int nvalid = warp_valid_rows(c, ctx);
+    const int row = c.row0 + r;
+    float gw = 0.0f;
+    if (row < c.row_end) {
+      const int t = __ldg(p.src_token + row);
+      if (t >= 0 && t < p.T) {
+        const int64_t base = static_cast<int64_t>(t) * p.k;
+#pragma unroll
+        for (int s = 0; s < kMaxTopK; ++s)
+          if (s < p.k && __ldg(p.row_of + base + s) == row) gw = __ldg(p.gate + base + s);
+      }
+    }
+    uint16_t* row_ptr = p.out + static_cast<int64_t>(row) * p.ld + c.n_blk * BN;
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int col = 0; col < BN; col += 32) {
+      float v[32];
+      __syncwarp();
+      tmem_ld32(taddr + col, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[col / 2 + j] = pack_bf16x2(gw * v[2 * j], gw * v[2 * j + 1]);
     }
     release_accumulator(ctx);
     if (nvalid > 0) {

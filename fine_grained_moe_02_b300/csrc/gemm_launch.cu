@@ -219,6 +219,20 @@ int launch_gemm2(const FfnArgs& a, cudaStream_t stream) {
   return run_gemm_bn<EpiStoreBf16>(bn, ta, tb, td, sh, ep, a.sm_count, stream, bn);
 }
 
+// Expert GEMM-2 with the gate folded into the epilogue:
+// y_perm[r] = gate[src_token[r], s] * (act Wd^T)[r], row_of[src_token[r], s] = r.
+int launch_gemm2_gated(const FfnArgs& a, cudaStream_t stream) {
+  CUtensorMap ta, tb, td;
+  const int rows = static_cast<int>(a.rows);
+  const int bn = pick_bn(a.d);
+  if (!make_tmap_bf16_2d(&ta, a.act, a.I, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&tb, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, bn)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&td, a.y_perm, a.d, a.rows, kBK, 32)) return MOE_ERR_CUDA;
+  GemmShape sh{a.I, a.I, a.d, a.E, a.offsets, rows, a.status};
+  EpiStoreGated::Params ep{a.y_perm, a.d, a.src_token, a.row_of, a.gate, a.T, a.k};
+  return run_gemm_bn<EpiStoreGated>(bn, ta, tb, td, sh, ep, a.sm_count, stream, bn);
+}
+
 // Self-test of the bounded waits: one 128 x 256 x 64 tile whose producer
 // issues nothing, so the MMA and epilogue waits run out after `limit_ns`.
 // Operands and output live in `scratch` (>= 112 KB); nothing is loaded or stored.

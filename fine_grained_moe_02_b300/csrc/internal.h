@@ -89,12 +89,17 @@ struct FfnArgs {
   int d, I, E;
   int* status;
   int sm_count;
+  // gate folded into expert GEMM-2 (launch_gemm2_gated): y_perm[r] is scaled by
+  // gate[t, s] for the pair (t, s) with row_of[t, s] = r, t = src_token[r]
+  const int32_t* row_of;     // [T, k]
+  const float* gate;         // [T, k]
+  int k;
 };
 
 struct CombineArgs {
   const uint16_t* y_perm;
   const int32_t* row_of;
-  const float* gate;
+  const float* gate;       // nullptr: rows already carry their gates (summed with weight 1)
   uint16_t* out;
   int64_t T;
   int d, k;
@@ -117,6 +122,7 @@ int launch_fold_router(const uint16_t* w_head, const uint16_t* w_lat, int E, int
                        cudaStream_t stream);
 int launch_gemm1(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm2(const FfnArgs& a, cudaStream_t stream);
+int launch_gemm2_gated(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream);
 int launch_combine(const CombineArgs& a, cudaStream_t stream);
 int launch_selftest_timeout(uint16_t* scratch, int* status, uint64_t limit_ns, cudaStream_t stream);

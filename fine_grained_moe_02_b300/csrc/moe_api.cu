@@ -575,6 +575,29 @@ int moe_expert_gemm2(const moe_dims* dims, const moe_bf16* act, const int32_t* o
   return launch_gemm2(a, static_cast<cudaStream_t>(stream));
 }
 
+int moe_expert_gemm2_gated(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets,
+                           const moe_bf16* w_down, const int32_t* src_token, const int32_t* row_of,
+                           const float* topk_gate, moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  FfnArgs a;
+  int rc = ffn_args(dims, offsets, ws, ws_bytes, a);
+  if (rc != MOE_OK) return rc;
+  if (act == nullptr || w_down == nullptr || src_token == nullptr || row_of == nullptr || topk_gate == nullptr ||
+      y_perm == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(act) || !aligned16(w_down) || !aligned16(src_token) || !aligned16(row_of) ||
+      !aligned16(topk_gate) || !aligned16(y_perm))
+    return MOE_ERR_MISALIGNED;
+  a.act = const_cast<moe_bf16*>(act);  // read only (TMA source)
+  a.w_down = w_down;
+  a.y_perm = y_perm;
+  a.src_token = src_token;
+  a.row_of = row_of;
+  a.gate = topk_gate;
+  a.T = dims->T;
+  a.k = dims->top_k;
+  return launch_gemm2_gated(a, static_cast<cudaStream_t>(stream));
+}
+
 int moe_expert_ffn(const moe_dims* dims, const moe_bf16* x_perm, const int32_t* offsets, const moe_bf16* w13,
                    const moe_bf16* w_down, moe_bf16* act, moe_bf16* y_perm, void* ws, size_t ws_bytes,
                    void* stream) {
@@ -614,10 +637,71 @@ int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row
   return launch_combine(a, static_cast<cudaStream_t>(stream));
 }
 
+int moe_combine_rows(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row_of, moe_bf16* out,
+                     void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (y_perm == nullptr || row_of == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(row_of) || !aligned16(out)) return MOE_ERR_MISALIGNED;
+  const int sms = sm_count_current();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  CombineArgs a{};
+  a.y_perm = y_perm;
+  a.row_of = row_of;
+  a.gate = nullptr;  // rows already scaled by their gates
+  a.out = out;
+  a.T = dims->T;
+  a.d = dims->d;
+  a.k = dims->top_k;
+  a.sm_count = sms;
+  return launch_combine(a, static_cast<cudaStream_t>(stream));
+}
+
 int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, void* ws,
                 size_t ws_bytes, void* stream) {
   return forward_impl(dims, x, w_lat, w_head, bias, w13, w_down, out, ws, ws_bytes, stream, true);
+}
+
+int moe_forward_fused(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                      const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, uint32_t fuse,
+                      void* ws, size_t ws_bytes, void* stream) {
+  int rc = moe_check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if ((fuse & ~static_cast<uint32_t>(MOE_FUSE_GATHER | MOE_FUSE_GATE)) != 0u) return MOE_ERR_INVALID_ARG;
+  if (x == nullptr || w_lat == nullptr || w_head == nullptr || w13 == nullptr || w_down == nullptr ||
+      out == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_lat) || !aligned16(w_head) || !aligned16(w13) || !aligned16(w_down) ||
+      !aligned16(out) || !aligned16(ws) || (bias != nullptr && !aligned16(bias)))
+    return MOE_ERR_MISALIGNED;
+  const ForwardLayout f = forward_layout(dims);
+  if (ws_bytes < f.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = moe_clear_device_status(ws, stream)) != MOE_OK) return rc;
+  int32_t* idx = at<int32_t>(ws, f.idx);
+  float* gate = at<float>(ws, f.gate);
+  int32_t* offsets = at<int32_t>(ws, f.offsets);
+  int32_t* row_of = at<int32_t>(ws, f.row_of);
+  int32_t* src = at<int32_t>(ws, f.src);
+  moe_bf16* yperm = at<moe_bf16>(ws, f.xperm);  // x_perm's region (x_perm itself not formed with the gather fused)
+  moe_bf16* act = at<moe_bf16>(ws, f.act);
+  if ((rc = moe_route(dims, x, w_lat, w_head, bias, idx, gate, nullptr, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  if (fuse & MOE_FUSE_GATHER) {
+    if ((rc = moe_dispatch_indices(dims, idx, offsets, row_of, src, ws, ws_bytes, stream)) != MOE_OK) return rc;
+    rc = moe_expert_gemm1_gather(dims, x, src, offsets, w13, act, ws, ws_bytes, stream);
+  } else {
+    if ((rc = moe_dispatch(dims, x, idx, offsets, row_of, src, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+    rc = moe_expert_gemm1(dims, yperm, offsets, w13, act, ws, ws_bytes, stream);
+  }
+  if (rc != MOE_OK) return rc;
+  if (fuse & MOE_FUSE_GATE) {
+    if ((rc = moe_expert_gemm2_gated(dims, act, offsets, w_down, src, row_of, gate, yperm, ws, ws_bytes, stream)) !=
+        MOE_OK)
+      return rc;
+    return moe_combine_rows(dims, yperm, row_of, out, stream);
+  }
+  if ((rc = moe_expert_gemm2(dims, act, offsets, w_down, yperm, ws, ws_bytes, stream)) != MOE_OK) return rc;
+  return moe_combine(dims, yperm, row_of, gate, out, stream);
 }
 
 int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,

@@ -132,6 +132,9 @@ int moe_prepare_weights(const moe_dims* dims, const moe_bf16* w_gate, const moe_
                         moe_bf16* w13, void* stream);
 
 /* Routing (latent projection, summed head scores, softmax, top-k, gates).
+ * Passage: "MAGI-2 Preview" (heyaiwiki), Architecture table, "Routing" row
+ * (multi-head latent routing, 12 heads x 256 dims, top-6); the expert
+ * routing step of the operator library in the 36kr article, section 02.
  *   x        [T, d] bf16
  *   w_lat    [n_heads*head_dim, d] bf16
  *   w_head   [E, n_heads*head_dim] bf16
@@ -190,6 +193,8 @@ int moe_route_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_
 
 /* Sorting: counting-sort permutation of the T*top_k (token, slot) pairs into
  * expert-contiguous order, then the row gather.
+ * Passage: the sorting step of the operator library (routing -> sorting ->
+ * calculation) in the 36kr article, section 02.
  *   topk_idx  [T, top_k] int32 (read)
  *   offsets   [E + 1] int32 (written): exclusive prefix of per-expert counts
  *   row_of    [T, top_k] int32 (written): destination row of (t, slot);
@@ -203,6 +208,8 @@ int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_id
                  void* ws, size_t ws_bytes, void* stream);
 
 /* Calculation: grouped SwiGLU expert GEMMs over ragged expert groups.
+ * Passage: the calculation step of the operator library in the 36kr article,
+ * section 02 (many small matrix products, one per fine-grained expert).
  *   x_perm  [T*top_k, d] bf16, rows of expert e are [offsets[e], offsets[e+1])
  *   offsets [E + 1] int32 device array (read on the device only)
  *   w13     [E, 2*inter, d] bf16 from moe_prepare_weights
@@ -260,16 +267,21 @@ int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t
  * copies by two extra warps of the GEMM kernel, so x_perm is never
  * materialised (saves T*top_k*d*2 bytes of memory and the gather's HBM round
  * trip).  The result equals moe_expert_gemm1 on the gathered x_perm bit for
- * bit.  On B300 it is ~1 ms slower on the clip workload than the separate
- * gather plus moe_expert_gemm1 (the copies are handed to the tensor core
- * stage by stage, two k-slices behind), so moe_forward does not use it. */
+ * bit.  moe_forward_fused with MOE_FUSE_GATHER runs it; on B300 that layer
+ * is ~1.7 ms slower on the clip workload than the separate gather plus
+ * moe_expert_gemm1 (19.2 against 17.5 ms: the copies are handed to the
+ * tensor core stage by stage, two k-slices behind), so moe_forward keeps
+ * the separate gather. */
 int moe_expert_gemm1_gather(const moe_dims* dims, const moe_bf16* x, const int32_t* src_token,
                             const int32_t* offsets, const moe_bf16* w13, moe_bf16* act, void* ws, size_t ws_bytes,
                             void* stream);
 int moe_expert_gemm2(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets, const moe_bf16* w_down,
                      moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream);
 
-/* Gate-weighted combine, scatter-free (one writer per output row):
+/* Gate-weighted combine, scatter-free (one writer per output row).
+ * Passage: the end of the routing -> sorting -> calculation chain in the
+ * 36kr article, section 02 (expert outputs brought back to token order and
+ * summed with the router's weights):
  *   out[t] = sum_{s < top_k} topk_gate[t, s] * y_perm[row_of[t, s]]
  * summed in slot order in fp32, rounded once to bf16.  A row index outside
  * [0, T*top_k) contributes nothing.
@@ -280,11 +292,47 @@ int moe_combine(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row
 
 /* The whole layer: moe_route, moe_dispatch, moe_expert_ffn, moe_combine on
  * one stream, intermediates in `ws` (at least moe_workspace_size bytes).
+ * Passage: MagiMoE in "MAGI-2 Preview" (heyaiwiki), FAQ "What is MagiMoE?",
+ * and the operator library of the 36kr article, section 02.
  * Clears the device status word first.  Weights: w13 from
  * moe_prepare_weights, w_down [E, d, inter]. */
 int moe_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out,
                 void* ws, size_t ws_bytes, void* stream);
+
+/* Fusions of the layer's steps (the 36kr article, section 02: the operator
+ * library fuses calculation steps to cut intermediate results and memory
+ * traffic).
+ *
+ * moe_expert_gemm2_gated: moe_expert_gemm2 with the gate multiply in its
+ * epilogue, y_perm[r] = bf16(topk_gate[t, s] * (act W_down^T)[r]) where
+ * t = src_token[r] and row_of[t, s] = r (so y is rounded to bf16 after the
+ * gate, not before).  src_token, row_of: from moe_dispatch; topk_gate from
+ * moe_route.  A row whose token does not list it gets gate 0.
+ *
+ * moe_combine_rows: out[t] = sum_{s < top_k} y_perm[row_of[t, s]] (rows
+ * already scaled by their gates), fp32 sum in slot order, one bf16 rounding.
+ *
+ * moe_forward_fused: moe_forward with a choice of fusions (fuse = OR of):
+ *   MOE_FUSE_GATHER  the sorting gather runs inside expert GEMM-1's operand
+ *                    loads (moe_dispatch_indices + moe_expert_gemm1_gather):
+ *                    x_perm is never written or read back
+ *   MOE_FUSE_GATE    the gate multiply runs in expert GEMM-2's epilogue
+ *                    (moe_expert_gemm2_gated + moe_combine_rows)
+ * fuse = 0 is moe_forward's sequence.  Unknown bits: MOE_ERR_INVALID_ARG.
+ * Same workspace as moe_forward; same outputs within the layer's
+ * tolerances (with MOE_FUSE_GATE the bf16 rounding of y_perm moves after
+ * the gate, so the bits differ from moe_forward's). */
+#define MOE_FUSE_GATHER 0x1u
+#define MOE_FUSE_GATE 0x2u
+int moe_expert_gemm2_gated(const moe_dims* dims, const moe_bf16* act, const int32_t* offsets,
+                           const moe_bf16* w_down, const int32_t* src_token, const int32_t* row_of,
+                           const float* topk_gate, moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream);
+int moe_combine_rows(const moe_dims* dims, const moe_bf16* y_perm, const int32_t* row_of, moe_bf16* out,
+                     void* stream);
+int moe_forward_fused(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_lat, const moe_bf16* w_head,
+                      const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, uint32_t fuse,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward with the folded router (w_router from moe_prepare_router). */
 int moe_forward_folded(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,

@@ -94,8 +94,13 @@ CONFIGS = {
     # experts, small enough (~1.5 GB on the device) for full profiler captures
     "slice": MoeConfig("slice", T=4096, d=4096, E=32, inter=1024,
                        note="profiling size: 4096 tokens, d=4096, E=32, inter=1024"),
+    # not one of the pages' workloads: the first 16384 tokens' worth of the clip
+    # workload (same width, experts and Zipf bias, about 4.6 GB on the device),
+    # small enough for counter captures whose DRAM bytes scale to the clip
+    "clip_slice": MoeConfig("clip_slice", T=16384, d=4096, E=128, inter=1024, bias="zipf",
+                            note="profiling size: 16384 tokens at the clip workload's width, experts and bias"),
 }
-CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "headlocal", "slice"]
+CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "headlocal", "slice", "clip_slice"]
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
