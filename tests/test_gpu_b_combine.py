@@ -16,7 +16,6 @@ def test_combine_matches_oracle(T, d, E, k):
     g = np.random.default_rng(T + d)
     idx = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
     _, _, row_of, _ = O.dispatch(idx, E)
-    y_u16 = G.small_inputs  # noqa (keeps import used)
     y32 = g.standard_normal((T * k, d)).astype(np.float32)
     yb = torch.from_numpy(y32).to(torch.bfloat16)
     gate = g.random((T, k)).astype(np.float32)

@@ -37,19 +37,17 @@ class HLDev:
 
 def _check(inp, out, idx, logits, tokens=None):
     cfg = inp["cfg"]
-    xw = O.widen_bf16(inp["x"] if tokens is None else inp["x"][tokens])
     idx_np = idx.cpu().numpy()
     lg = logits.cpu().numpy()
     if tokens is not None:
         idx_np, lg = idx_np[:, tokens], lg[:, tokens]
-    for j in range(cfg.n_heads):
-        s_ref = xw[:, j * cfg.head_dim:(j + 1) * cfg.head_dim] @ O.widen_bf16(inp["w_router"][j]).T
-        if inp["bias"] is not None:
-            s_ref = s_ref + np.asarray(inp["bias"][j], dtype=np.float64)[None, :]
-        p = O.softmax(s_ref)
-        gates = O.renormalised_gates(p, idx_np[j])
-        G.check_routing(s_ref, idx_np[j], gates.astype(np.float32), cfg.top_k, lg[j])
     ref = O.forward_bits(inp, tokens=tokens, topk_idx=idx_np)
+    for j in range(cfg.n_heads):
+        # each head's scores from the oracle; the layer returns no gates, so
+        # the gate check is the oracle's own renormalisation of the GPU's ids
+        s_ref = ref["logits"][j]
+        gates = O.renormalised_gates(O.softmax(s_ref), idx_np[j])
+        G.check_routing(s_ref, idx_np[j], gates.astype(np.float32), cfg.top_k, lg[j])
     got = G.host_f64(out if tokens is None else out[torch.from_numpy(tokens).cuda()])
     return G.check_out(got, ref["out"])
 
