@@ -3,12 +3,18 @@
 // This is the "sorting" step of the MagiMoE operator library ("Sand.ai: The world's first 100-billion-parameter open-source MoE video generation model MAGI Preview" (36kr), section "02. Two Key Technical Decision Points").
 //
 //   1. hist    : per token block, per-expert counts            (blocks of kTokBlock tokens)
-//   2. scan    : per expert, exclusive prefix over blocks; offsets = exclusive prefix
-//                over experts of the totals                    (one CTA)
-//   3. assign  : row of (t, e) = offsets[e] + #{t' < t : t' chose e}; within a block
-//                the rank comes from per-warp bitmasks, so the order is fixed by
-//                the token index and never by the order of atomics
-//   4. gather  : one warp per token reads x[t] once and writes it to its k rows
+//   2. assign  : each block first forms its own bases from all blocks' counts
+//                (per expert, the counts of earlier blocks plus the exclusive
+//                prefix over experts of the totals = offsets; block 0 writes
+//                offsets), then row of (t, e) = offsets[e] + #{t' < t : t' chose e};
+//                within a block the rank comes from per-warp bitmasks, so the
+//                order is fixed by the token index and never by the order of atomics
+//   3. gather  : one warp per token reads x[t] once and writes it to its k rows
+// The three are chained with programmatic dependent launch: each kernel lets
+// the next one be scheduled as soon as all of its blocks are running, and
+// waits (griddepcontrol.wait) for its predecessor's completion and memory
+// before touching anything the predecessor writes or reads, so a kernel's
+// launch and ramp overlap the previous kernel's tail.
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -16,6 +22,12 @@
 #include "moe.h"
 
 namespace moe {
+
+// Programmatic dependent launch: wait for the preceding grid (a no-op when
+// this grid was launched without the attribute), and let the next grid be
+// scheduled once every block of this one has reached this point.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 constexpr int kTokBlock = 2048;   // tokens per hist/assign block
 constexpr int kAssignWarps = 16;  // warps per assign block; each owns kTokBlock/16 tokens
@@ -41,6 +53,8 @@ __device__ __forceinline__ void load_slots(const int32_t* __restrict__ row, int 
 __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k,
                                                             int E, int32_t* __restrict__ block_counts,
                                                             int* status) {
+  pdl_wait();
+  pdl_trigger();
   // head blockIdx.y of a batch of independent sorts
   topk_idx += static_cast<int64_t>(blockIdx.y) * T * k;
   block_counts += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
@@ -63,69 +77,60 @@ __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __res
     block_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One CTA of 1024 threads.  block_base[b, e] = offsets[e] + sum_{b' < b} counts[b', e].
-__global__ void __launch_bounds__(1024) dispatch_scan_kernel(const int32_t* __restrict__ block_counts, int nblk,
-                                                             int E, int32_t* __restrict__ block_base,
-                                                             int32_t* __restrict__ offsets) {
-  // head blockIdx.x of a batch of independent sorts
-  block_counts += static_cast<int64_t>(blockIdx.x) * nblk * E;
-  block_base += static_cast<int64_t>(blockIdx.x) * nblk * E;
-  offsets += static_cast<int64_t>(blockIdx.x) * (E + 1);
-  __shared__ int total[kMaxExperts];
-  __shared__ int off[kMaxExperts + 1];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  for (int e = warp; e < E; e += nwarps) {
-    int carry = 0;
-    for (int b0 = 0; b0 < nblk; b0 += 32) {
-      const int b = b0 + lane;
-      const int v = (b < nblk) ? block_counts[static_cast<int64_t>(b) * E + e] : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (b < nblk) block_base[static_cast<int64_t>(b) * E + e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) total[e] = carry;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int v = (e < E) ? total[e] : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (e < E) off[e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) off[E] = carry;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
-  for (int64_t i = threadIdx.x; i < static_cast<int64_t>(nblk) * E; i += blockDim.x)
-    block_base[i] += off[i % E];
-}
-
 // kAssignWarps warps; warp w owns tokens [t0 + w*span, t0 + (w+1)*span) of the block.
 __global__ void __launch_bounds__(kAssignWarps * 32) dispatch_assign_kernel(
-    const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, const int32_t* __restrict__ block_base,
-    int32_t* __restrict__ row_of, int32_t* __restrict__ src_token) {
+    const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, const int32_t* __restrict__ block_counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ src_token) {
+  pdl_wait();
+  pdl_trigger();
   // head blockIdx.y of a batch of independent sorts
   topk_idx += static_cast<int64_t>(blockIdx.y) * T * k;
-  block_base += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
+  block_counts += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
+  offsets += static_cast<int64_t>(blockIdx.y) * (E + 1);
   row_of += static_cast<int64_t>(blockIdx.y) * T * k;
   src_token += static_cast<int64_t>(blockIdx.y) * T * k;
   __shared__ int wcnt[kAssignWarps][kMaxExperts];   // per-warp counts, then per-warp cursors
   __shared__ unsigned mask[kAssignWarps][kMaxExperts];
+  __shared__ int s_base[kMaxExperts];                // this block's first row of each expert
+  __shared__ int s_off[kMaxExperts + 1];             // offsets (exclusive prefix of the totals)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = static_cast<int>(gridDim.x);
+
+  // this block's bases: per expert the counts of the blocks before it, and
+  // the totals over all blocks (every block forms the same totals)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int pre = 0, tot = 0;
+#pragma unroll 4
+    for (int b = 0; b < nblk; ++b) {
+      const int c = __ldg(block_counts + static_cast<int64_t>(b) * E + e);
+      tot += c;
+      pre += (b < static_cast<int>(blockIdx.x)) ? c : 0;
+    }
+    s_base[e] = pre;
+    s_off[e] = tot;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix over experts of the totals
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = (e < E) ? s_off[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) s_off[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_off[E] = carry;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    if (e < E) s_base[e] += s_off[e];
+    if (blockIdx.x == 0) offsets[e] = s_off[e];
+  }
   constexpr int span = kTokBlock / kAssignWarps;
   const int64_t tb = static_cast<int64_t>(blockIdx.x) * kTokBlock;
   const int64_t w0 = tb + warp * span;
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(kAssignWarps * 32) dispatch_assign_kernel(
   __syncthreads();
   // exclusive prefix over warps, seeded with the block's global base
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = block_base[static_cast<int64_t>(blockIdx.x) * E + e];
+    int run = s_base[e];
     for (int w = 0; w < kAssignWarps; ++w) {
       const int c = wcnt[w][e];
       wcnt[w][e] = run;
@@ -207,6 +212,8 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
                                                               int64_t x_ld_vec, int64_t x_head_vec, int heads, int k,
                                                               const int32_t* __restrict__ row_of, int64_t rows,
                                                               uint4* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -238,28 +245,49 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
   }
 }
 
+// Launches `kern` with programmatic stream serialization: it may be scheduled
+// while the previous kernel on the stream is still running (it waits for it
+// with griddepcontrol.wait).
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, cudaStream_t stream, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+}
+
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   const int nblk = static_cast<int>((a.T + kTokBlock - 1) / kTokBlock);
   const int heads = a.heads > 1 ? a.heads : 1;
-  dispatch_hist_kernel<<<dim3(nblk, heads), 256, 0, stream>>>(a.topk_idx, a.T, a.k, a.E, a.block_counts, a.status);
-  dispatch_scan_kernel<<<heads, 1024, 0, stream>>>(a.block_counts, nblk, a.E, a.block_base, a.offsets);
-  dispatch_assign_kernel<<<dim3(nblk, heads), kAssignWarps * 32, 0, stream>>>(a.topk_idx, a.T, a.k, a.E,
-                                                                               a.block_base, a.row_of, a.src_token);
+  if (launch_pdl(dispatch_hist_kernel, dim3(nblk, heads), dim3(256), stream, a.topk_idx, a.T, a.k, a.E,
+                 a.block_counts, a.status) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_pdl(dispatch_assign_kernel, dim3(nblk, heads), dim3(kAssignWarps * 32), stream, a.topk_idx, a.T, a.k,
+                 a.E, a.block_counts, a.offsets, a.row_of, a.src_token) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (a.x_perm != nullptr) {
     const int d_vec = a.d / 8;
     const int64_t want = (a.T * heads + 7) / 8;  // 8 warps (tokens) per CTA
     const int grid = static_cast<int>(want < a.sm_count * 8LL ? want : a.sm_count * 8LL);
     const int64_t x_ld_vec = (a.x_ld ? a.x_ld : a.d) / 8;
-    dispatch_gather_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(a.x), a.T, d_vec, x_ld_vec,
-                                                     a.x_head_off / 8, heads, a.k, a.row_of, a.T * a.k,
-                                                     reinterpret_cast<uint4*>(a.x_perm));
+    if (launch_pdl(dispatch_gather_kernel, dim3(grid), dim3(256), stream, reinterpret_cast<const uint4*>(a.x), a.T,
+                   d_vec, x_ld_vec, a.x_head_off / 8, heads, a.k, a.row_of, a.T * a.k,
+                   reinterpret_cast<uint4*>(a.x_perm)) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 size_t dispatch_scratch_bytes(int64_t T, int E) {
   const int64_t nblk = (T + kTokBlock - 1) / kTokBlock;
-  return static_cast<size_t>(2 * nblk * E) * sizeof(int32_t);
+  return static_cast<size_t>(nblk * E) * sizeof(int32_t);
 }
 
 size_t dispatch_counter_cells(int64_t T, int E) { return static_cast<size_t>((T + kTokBlock - 1) / kTokBlock) * E; }

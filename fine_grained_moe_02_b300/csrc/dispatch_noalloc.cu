@@ -11,12 +11,12 @@
 
 namespace {
 
-// Per-block expert counters and bases, ceil(T / 2048) * E cells each.
+// Per-block expert counters, ceil(T / 2048) * E cells.
 constexpr int64_t kNoAllocMaxCells = 65536;
 constexpr int64_t kSinkInts = 64;  // status sink when the caller passes no status word
 
 // Lives for as long as the library is loaded, on every GPU that loads it.
-static __device__ __align__(256) int32_t g_dispatch_scratch[kSinkInts + 2 * kNoAllocMaxCells];
+static __device__ __align__(256) int32_t g_dispatch_scratch[kSinkInts + kNoAllocMaxCells];
 
 // Device address of g_dispatch_scratch in the current context.  Host code may
 // not use the symbol itself (on the host it names a stand-in, not device
@@ -47,8 +47,8 @@ extern "C" int moe_dispatch_noalloc(const moe_dims* dims, const moe_bf16* x, con
   if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(offsets) || !aligned16(row_of) ||
       !aligned16(src_token) || !aligned16(x_perm) || (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u)))
     return MOE_ERR_MISALIGNED;
-  // the counters need ceil(T / 2048) * E cells of each kind
-  const int64_t cells = static_cast<int64_t>(moe::dispatch_scratch_bytes(dims->T, dims->E) / (2 * sizeof(int32_t)));
+  // the counters need ceil(T / 2048) * E cells
+  const int64_t cells = static_cast<int64_t>(moe::dispatch_counter_cells(dims->T, dims->E));
   if (cells > kNoAllocMaxCells) return MOE_ERR_UNSUPPORTED_SHAPE;
 
   int32_t* scratch = nullptr;
@@ -59,8 +59,8 @@ extern "C" int moe_dispatch_noalloc(const moe_dims* dims, const moe_bf16* x, con
     return MOE_ERR_CUDA;
 
   // Every cell the kernels read is written earlier in the same call (the
-  // histogram pass writes all counters, the scan writes all bases), so
-  // nothing is cleared; the sink word is written but never read.
+  // histogram pass writes all counters before the assign pass reads them),
+  // so nothing is cleared; the sink word is written but never read.
   moe::DispatchArgs a{};
   a.x = x;
   a.topk_idx = topk_idx;
@@ -73,7 +73,6 @@ extern "C" int moe_dispatch_noalloc(const moe_dims* dims, const moe_bf16* x, con
   a.src_token = src_token;
   a.x_perm = x_perm;
   a.block_counts = scratch + kSinkInts;
-  a.block_base = scratch + kSinkInts + kNoAllocMaxCells;
   a.status = status != nullptr ? status : scratch;
   a.sm_count = sms;
   return moe::launch_dispatch(a, static_cast<cudaStream_t>(stream));

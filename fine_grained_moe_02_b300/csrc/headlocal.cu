@@ -43,7 +43,7 @@ struct HlLayout {
 
 // Per-head arrays side by side: idx/gate/row_of/src [H, T, k], offsets [H, E+1],
 // x_perm (then y_perm) [H, T*k, head_dim], act [H, T*k, inter], dispatch
-// counters [2][H][nblk][E]; goff [H*E + 1]: the group offsets of all heads'
+// counters [H][nblk][E]; goff [H*E + 1]: the group offsets of all heads'
 // experts over the concatenated rows (head h's rows start at h*T*k).
 HlLayout hl_layout(const moe_dims* d) {
   HlLayout l;
@@ -147,7 +147,6 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
   da.src_token = at<int32_t>(ws, l.src);
   da.x_perm = at<uint16_t>(ws, l.xperm);
   da.block_counts = at<int32_t>(ws, l.disp);
-  da.block_base = at<int32_t>(ws, l.disp) + static_cast<int64_t>(H) * dispatch_counter_cells(T, E);
   da.status = status;
   da.sm_count = sms;
   if ((rc = launch_dispatch(da, s)) != MOE_OK) return rc;

@@ -43,8 +43,7 @@ struct DispatchArgs {
   // block counters.  heads <= 1: one sort.
   int heads;
   int64_t x_head_off;
-  int32_t* block_counts;   // scratch [nblk * E]
-  int32_t* block_base;     // scratch [nblk * E]
+  int32_t* block_counts;   // scratch [nblk * E]: per-block expert counts
   int* status;
   int sm_count;
 };
@@ -112,7 +111,7 @@ struct CombineArgs {
 
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream);
 size_t dispatch_scratch_bytes(int64_t T, int E);
-size_t dispatch_counter_cells(int64_t T, int E);  // ceil(T / block) * E: one of the two counter arrays
+size_t dispatch_counter_cells(int64_t T, int E);  // ceil(T / block) * E: the per-block counters
 int launch_route(const RouteArgs& a, cudaStream_t stream);
 int launch_route_two_stage(const RouteArgs& a, cudaStream_t stream);
 bool route_fused_supported(int head_dim);

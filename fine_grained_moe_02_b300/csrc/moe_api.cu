@@ -33,7 +33,7 @@ int sm_count_current() {
 
 // Scratch layout (offsets from ws):
 //   [0, 1024)                  status word (int32 at 0)
-//   dispatch counters          2 * nblk * E int32
+//   dispatch counters          nblk * E int32
 //   hl                         T * 2L bf16 (router latent hi | lo)
 struct ScratchLayout {
   size_t disp, hl, end;
@@ -456,7 +456,6 @@ int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_id
   if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int sms = sm_count_current();
   if (sms <= 0) return MOE_ERR_CUDA;
-  const int64_t nblk_e = static_cast<int64_t>(dispatch_scratch_bytes(dims->T, dims->E) / 8);
   DispatchArgs a{};
   a.x = x;
   a.topk_idx = topk_idx;
@@ -469,7 +468,6 @@ int moe_dispatch(const moe_dims* dims, const moe_bf16* x, const int32_t* topk_id
   a.src_token = src_token;
   a.x_perm = x_perm;
   a.block_counts = at<int32_t>(ws, sl.disp);
-  a.block_base = at<int32_t>(ws, sl.disp) + nblk_e;
   a.status = status_ptr(ws);
   a.sm_count = sms;
   return launch_dispatch(a, static_cast<cudaStream_t>(stream));
@@ -487,7 +485,6 @@ int moe_dispatch_indices(const moe_dims* dims, const int32_t* topk_idx, int32_t*
   if (ws_bytes < sl.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int sms = sm_count_current();
   if (sms <= 0) return MOE_ERR_CUDA;
-  const int64_t nblk_e = static_cast<int64_t>(dispatch_scratch_bytes(dims->T, dims->E) / 8);
   DispatchArgs a{};
   a.topk_idx = topk_idx;
   a.T = dims->T;
@@ -499,7 +496,6 @@ int moe_dispatch_indices(const moe_dims* dims, const int32_t* topk_idx, int32_t*
   a.src_token = src_token;
   a.x_perm = nullptr;
   a.block_counts = at<int32_t>(ws, sl.disp);
-  a.block_base = at<int32_t>(ws, sl.disp) + nblk_e;
   a.status = status_ptr(ws);
   a.sm_count = sms;
   return launch_dispatch(a, static_cast<cudaStream_t>(stream));

@@ -236,8 +236,8 @@ int moe_dispatch_indices(const moe_dims* dims, const int32_t* topk_idx, int32_t*
  * inference runtimes), or latency-critical loops where an allocation's
  * implicit device synchronisation is not acceptable.  This variant takes no
  * workspace and allocates nothing: its counters live in a fixed array inside
- * libmoe's device image, 64 + 2 * 65536 int32 (about 512 KiB), which every
- * GPU that loads the library holds until the process exits.
+ * libmoe's device image, 64 + 65536 int32 (about 256 KiB), which every GPU
+ * that loads the library holds until the process exits.
  *   - Arguments and results as in moe_dispatch (same kernels, same output).
  *   - status: optional device int32 that receives MOE_DEV_* bits (OR-ed in;
  *     the caller clears it).  NULL: device-detected problems are not reported.
