@@ -110,6 +110,7 @@ _SIGS = {
     "moe_workspace_size_headlocal": (ctypes.c_int, [_DP, ctypes.POINTER(ctypes.c_size_t)]),
     "moe_prepare_weights_headlocal": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "moe_forward_headlocal": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward_headlocal_staged": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_forward_host": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
@@ -461,7 +462,9 @@ def moe_prepare_weights_headlocal(dims, w_gate, w_up, w13, stream=None) -> None:
                                                _stream(stream)), "moe_prepare_weights_headlocal")
 
 
-def moe_forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, logits, ws, stream=None) -> None:
+def moe_forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, logits, ws, stream=None,
+                          staged=False) -> None:
+    """staged=True: moe_forward_headlocal_staged (separate expert GEMMs)."""
     H, E, Dh, I, T, k = dims.n_heads, dims.E, dims.head_dim, dims.inter, dims.T, dims.top_k
     _need_n(x=(x, T * dims.d), w_router=(w_router, H * E * Dh), bias=(bias, H * E), w13=(w13, H * E * 2 * I * Dh),
             w_down=(w_down, H * E * Dh * I), out=(out, T * dims.d), topk_idx=(topk_idx, H * T * k),
@@ -469,9 +472,9 @@ def moe_forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, l
     _dev(x, w_router, w13, w_down, out, dtype=torch.bfloat16)
     _dev(bias, logits, dtype=torch.float32)
     _dev(topk_idx, dtype=torch.int32)
-    _check(lib().moe_forward_headlocal(ctypes.byref(dims), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w13),
-                                       _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(logits), _ptr(ws), ws.numel(),
-                                       _stream(stream)), "moe_forward_headlocal")
+    name = "moe_forward_headlocal_staged" if staged else "moe_forward_headlocal"
+    _check(getattr(lib(), name)(ctypes.byref(dims), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w13), _ptr(w_down),
+                                _ptr(out), _ptr(topk_idx), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), name)
 
 
 def moe_forward_host(dims, x_host, w_lat, w_head, bias, w13, w_down, out_host, ws, stream=None) -> None:

@@ -17,7 +17,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 LIB = PKG / "libmoe.so"
 BUILD_DIR = ROOT / "_build"
-SOURCES = ["moe_api.cu", "gemm_launch.cu", "dispatch.cu", "combine.cu", "dispatch_noalloc.cu", "router_fold.cu", "router_fused.cu", "headlocal.cu"]
+SOURCES = ["moe_api.cu", "gemm_launch.cu", "dispatch.cu", "combine.cu", "dispatch_noalloc.cu", "router_fold.cu", "router_fused.cu", "headlocal.cu", "ffn_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -38,13 +38,14 @@ int check_hl(const moe_dims* d) {
 }
 
 struct HlLayout {
-  size_t disp, idx, gate, offsets, goff, row_of, src, xperm, act, end;
+  size_t disp, idx, gate, offsets, goff, tiles, row_of, src, xperm, act, end;
 };
 
 // Per-head arrays side by side: idx/gate/row_of/src [H, T, k], offsets [H, E+1],
 // x_perm (then y_perm) [H, T*k, head_dim], act [H, T*k, inter], dispatch
 // counters [H][nblk][E]; goff [H*E + 1]: the group offsets of all heads'
-// experts over the concatenated rows (head h's rows start at h*T*k).
+// experts over the concatenated rows (head h's rows start at h*T*k); tiles
+// [H*E + 1]: the fused expert kernel's table of the groups' tile counts.
 HlLayout hl_layout(const moe_dims* d) {
   HlLayout l;
   const size_t H = d->n_heads;
@@ -54,7 +55,8 @@ HlLayout hl_layout(const moe_dims* d) {
   l.gate = align_up(l.idx + H * Tk * 4, kAlign);
   l.offsets = align_up(l.gate + H * Tk * 4, kAlign);
   l.goff = align_up(l.offsets + H * (static_cast<size_t>(d->E) + 1) * 4, kAlign);
-  l.row_of = align_up(l.goff + (H * d->E + 1) * 4, kAlign);
+  l.tiles = align_up(l.goff + (H * d->E + 1) * 4, kAlign);
+  l.row_of = align_up(l.tiles + (H * d->E + 1) * 4, kAlign);
   l.src = align_up(l.row_of + H * Tk * 4, kAlign);
   l.xperm = align_up(l.src + H * Tk * 4, kAlign);
   l.act = align_up(l.xperm + H * Tk * d->head_dim * 2, kAlign);
@@ -101,9 +103,15 @@ int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, 
                             static_cast<cudaStream_t>(stream));
 }
 
-int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
-                          const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx,
-                          float* logits, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The head-local layer; `staged` runs the two expert GEMMs as separate
+// grouped GEMMs (act through HBM) instead of the fused expert kernel.
+int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                      const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx, float* logits,
+                      void* ws, size_t ws_bytes, void* stream, bool staged) {
   int rc = check_hl(dims);
   if (rc != MOE_OK) return rc;
   if (x == nullptr || w_router == nullptr || w13 == nullptr || w_down == nullptr || out == nullptr || ws == nullptr)
@@ -160,12 +168,28 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
   fa.status = status;
   fa.sm_count = sms;
   uint16_t* act = at<uint16_t>(ws, l.act);
-  if (static_cast<int64_t>(H) * E <= kMaxGemmGroups) {
+  const bool fused = !staged && ffn_fused_supported(Dh, I);
+  if (fused || static_cast<int64_t>(H) * E <= kMaxGemmGroups) {
     int32_t* goff = at<int32_t>(ws, l.goff);
     const int64_t n = static_cast<int64_t>(H) * E + 1;
     const int blocks = static_cast<int>((n + 255) / 256 < sms ? (n + 255) / 256 : sms);
     concat_offsets_kernel<<<blocks, 256, 0, s>>>(da.offsets, H, E, Tk, goff);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (fused) {  // both expert layers in one kernel, act never leaves the SM
+      fa.offsets = goff;
+      fa.rows = static_cast<int64_t>(H) * Tk;
+      fa.E = H * E;
+      fa.x_perm = da.x_perm;
+      fa.w13 = w13;
+      fa.w_down = w_down;
+      fa.y_perm = da.x_perm;  // each tile reads its x rows before it writes their y rows
+      fa.tiles = at<int32_t>(ws, l.tiles);
+      if ((rc = launch_ffn_fused(fa, s)) != MOE_OK) return rc;
+    }
+  }
+  if (fused) {
+  } else if (static_cast<int64_t>(H) * E <= kMaxGemmGroups) {
+    int32_t* goff = at<int32_t>(ws, l.goff);
     fa.offsets = goff;
     fa.rows = static_cast<int64_t>(H) * Tk;
     fa.E = H * E;
@@ -204,6 +228,24 @@ int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf1
   ca.k = k;
   ca.sm_count = sms;
   return launch_combine(ca, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
+                          const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx,
+                          float* logits, void* ws, size_t ws_bytes, void* stream) {
+  return forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, logits, ws, ws_bytes, stream,
+                           false);
+}
+
+int moe_forward_headlocal_staged(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router,
+                                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out,
+                                 int32_t* topk_idx, float* logits, void* ws, size_t ws_bytes, void* stream) {
+  return forward_headlocal(dims, x, w_router, bias, w13, w_down, out, topk_idx, logits, ws, ws_bytes, stream,
+                           true);
 }
 
 }  // extern "C"

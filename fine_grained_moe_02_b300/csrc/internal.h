@@ -93,6 +93,7 @@ struct FfnArgs {
   const int32_t* row_of;     // [T, k]
   const float* gate;         // [T, k]
   int k;
+  int32_t* tiles;            // scratch [E + 1] (the fused expert kernel's tile table)
 };
 
 struct CombineArgs {
@@ -123,6 +124,11 @@ int launch_gemm1(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm2(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm2_gated(const FfnArgs& a, cudaStream_t stream);
 int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream);
+// Both expert GEMMs of narrow experts (d <= 256) in one kernel, act kept on chip:
+// y_perm = (silu(x_perm W_gate^T) * (x_perm W_up^T)) W_down^T; reads x_perm, offsets,
+// w13, w_down, rows, d, I, E (groups); no group limit.
+bool ffn_fused_supported(int D, int I);
+int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream);
 int launch_combine(const CombineArgs& a, cudaStream_t stream);
 int launch_selftest_timeout(uint16_t* scratch, int* status, uint64_t limit_ns, cudaStream_t stream);
 int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w13, int E, int I, int d,

@@ -397,15 +397,23 @@ int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x,
  *   logits [n_heads, T, E] fp32 or NULL (written: each head's scores)
  * Rules: head_dim % 64 == 0, inter % 64 == 0, E <= 256, top_k <= min(8, E).
  * All heads' routers run as one batched GEMM, their sorts, gathers and
- * combines as single launches over (head, token), each expert layer as one
- * grouped GEMM over all n_heads * E experts (head by head when
- * n_heads * E > 3072), all on `stream`. */
+ * combines as single launches over (head, token), all on `stream`.  With
+ * head_dim <= 256 both expert layers of all n_heads * E head-local experts
+ * run as one fused kernel that keeps each 128-row tile's activations on chip
+ * (the gate/up products in tensor memory, SwiGLU into shared memory, the
+ * down projection accumulating in tensor memory): the act intermediate never
+ * reaches HBM.  moe_forward_headlocal_staged runs the same layer with the two
+ * expert layers as separate grouped GEMMs (act through the workspace; head
+ * by head when n_heads * E > 3072); both give the same bits. */
 int moe_workspace_size_headlocal(const moe_dims* dims, size_t* bytes);
 int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
                                   void* stream);
 int moe_forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router, const float* bias,
                           const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out, int32_t* topk_idx,
                           float* logits, void* ws, size_t ws_bytes, void* stream);
+int moe_forward_headlocal_staged(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w_router,
+                                 const float* bias, const moe_bf16* w13, const moe_bf16* w_down, moe_bf16* out,
+                                 int32_t* topk_idx, float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward for a caller whose activations live in host memory: x_host
  * [T, d] in, out_host [T, d] out, weights on the device; returns after the

@@ -24,14 +24,14 @@ class HLDev:
         moe.moe_prepare_weights_headlocal(self.dims, G.dev_bf16(inp["w_gate"]), G.dev_bf16(inp["w_up"]), self.w13)
         self.ws = moe.alloc_workspace(moe.moe_workspace_size_headlocal(self.dims))
 
-    def forward(self):
+    def forward(self, staged=False):
         c = self.cfg
         out = torch.empty((c.T, c.d), dtype=torch.bfloat16, device="cuda")
         idx = torch.empty((c.n_heads, c.T, c.top_k), dtype=torch.int32, device="cuda")
         logits = torch.empty((c.n_heads, c.T, c.E), dtype=torch.float32, device="cuda")
         bias = None if self.inp["bias"] is None else torch.from_numpy(np.ascontiguousarray(self.inp["bias"])).cuda()
         moe.moe_forward_headlocal(self.dims, self.x, self.w_router, bias, self.w13, self.w_down, out, idx, logits,
-                                  self.ws)
+                                  self.ws, staged=staged)
         return out, idx, logits
 
 
@@ -94,3 +94,24 @@ def test_headlocal_per_head_router_bias():
     inp0["bias"] = None
     _, idx0, _ = HLDev(inp0).forward()
     assert not torch.equal(idx, idx0)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=300, d=128, n_heads=2, head_dim=64, E=8, inter=64, top_k=2),
+    dict(T=1000, d=512, n_heads=4, head_dim=128, E=32, inter=128, top_k=6),
+    dict(T=129, d=768, n_heads=3, head_dim=256, E=256, inter=64, top_k=8),
+    dict(T=700, d=768, n_heads=3, head_dim=256, E=40, inter=512, top_k=6),
+    dict(T=200, d=1024, n_heads=16, head_dim=64, E=256, inter=64, top_k=2),   # 4096 experts: staged head by head
+])
+def test_fused_expert_kernel_gives_the_staged_bits(kw):
+    # the fused expert kernel rounds act to bf16 exactly where the separate
+    # GEMMs do and runs the same MMA sequence: identical outputs
+    inp = mi.make_inputs(mi.custom_config("hlf", head_local=True, **kw))
+    dev = HLDev(inp)
+    out, idx, _ = dev.forward()
+    assert moe.moe_get_device_status(dev.ws) == 0
+    ref, idx2, _ = dev.forward(staged=True)
+    assert moe.moe_get_device_status(dev.ws) == 0
+    assert torch.equal(idx, idx2)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    _check(inp, out, idx, _)
