@@ -507,15 +507,22 @@ def main():
     r1.record(stream)
     barrier()
     fold_route_ms = r0.elapsed_time(r1) / n_fold
-    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    moe.moe_route_fused(dims, x, w_lat, w_head, bias, idx, gate, None, ws)
-    barrier()
-    q0.record(stream)
-    for _ in range(n_fold):
+    # the two routers of the latent path, interleaved (one call each per round)
+    rt = {"two_stage": [], "on_chip": []}
+    for _ in range(2):
+        moe.moe_route_two_stage(dims, x, w_lat, w_head, bias, idx, gate, None, ws)
         moe.moe_route_fused(dims, x, w_lat, w_head, bias, idx, gate, None, ws)
-    q1.record(stream)
     barrier()
-    fused_route_ms = q0.elapsed_time(q1) / n_fold
+    for _ in range(n_fold):
+        for name, fn in (("two_stage", moe.moe_route_two_stage), ("on_chip", moe.moe_route_fused)):
+            e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            e[0].record(stream)
+            fn(dims, x, w_lat, w_head, bias, idx, gate, None, ws)
+            e[1].record(stream)
+            rt[name].append(e)
+    barrier()
+    fused_route_ms = statistics.mean(a.elapsed_time(b) for a, b in rt["on_chip"])
+    two_stage_route_ms = statistics.mean(a.elapsed_time(b) for a, b in rt["two_stage"])
     if moe.moe_get_device_status(ws) != 0:
         raise SystemExit("device status set by a router variant")
 
@@ -645,8 +652,9 @@ def main():
             "on_chip_router": {
                 "route_ms": fused_route_ms,
                 "router_tflops": alg["router_flops"] / (fused_route_ms * 1e-3) / 1e12,
+                "two_stage_route_ms": two_stage_route_ms,
                 "path": "moe_route_fused: latent h kept in tensor memory, head-group partial scores only; "
-                        "timed on its own (the step uses moe_route)"}},
+                        "timed in rounds interleaved with moe_route_two_stage"}},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "gpu_launches_note": "launches of libmoe kernels inside the timed step loop (route 2, sort 4, expert GEMMs 2, "
                              "combine 1 per step)",
