@@ -37,7 +37,7 @@ sys.path.insert(0, str(ROOT))
 import moe_inputs as mi  # noqa: E402
 
 METRIC = "MoE-layer tokens/sec on 1 B300; grouped-GEMM % bf16 TC peak; permute GB/s"
-KERNELS_PER_STEP = 9  # 2 router GEMMs, 4 sorting kernels, 2 expert GEMMs, combine
+KERNELS_PER_STEP = 8  # 2 router GEMMs, 3 sorting kernels, 2 expert GEMMs, combine
 GEMM_SOURCES = ["gemm_tc.cuh", "epilogues.cuh", "ptx.cuh", "gemm_launch.cu"]
 NOMINAL_BF16_TFLOPS = 2250.0   # B300 dense bf16 at its maximum SM clock
 NOMINAL_SM_MHZ = 2032.0
@@ -656,7 +656,7 @@ def main():
                 "path": "moe_route_fused: latent h kept in tensor memory, head-group partial scores only; "
                         "timed in rounds interleaved with moe_route_two_stage"}},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
-        "gpu_launches_note": "launches of libmoe kernels inside the timed step loop (route 2, sort 4, expert GEMMs 2, "
+        "gpu_launches_note": "launches of libmoe kernels inside the timed step loop (route 2, sort 3, expert GEMMs 2, "
                              "combine 1 per step)",
         "clocks": clk,
         "e2e": e2e,
