@@ -41,3 +41,22 @@ def test_full_size_workload(name, n_sample):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     if name == "clip":   # the skew the workload asks for
         assert counts.max() >= 0.9 * cfg.T and counts.min() > 0
+
+
+@pytest.mark.parametrize("fuse", [1, 2, 3])
+def test_full_clip_fused_forward_sampled(fuse):
+    # moe_forward_fused at the clip size, each fusion choice: sampled tokens
+    # against the oracle; with the gather fused alone, the bits of moe_forward
+    inp = mi.make_inputs("clip")
+    cfg = inp["cfg"]
+    dev = G.Dev(inp)
+    idx, _, _ = dev.route(want_logits=False)
+    out = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    import fine_grained_moe_02_b300 as moe
+    moe.moe_forward_fused(dev.dims, dev.x, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, out, fuse, dev.ws)
+    assert dev.status() == 0
+    tok = mi.sample_tokens(cfg.T, 128, seed=23 + fuse)
+    ref = O.forward_bits(inp, tokens=tok, topk_idx=idx.cpu().numpy()[tok])
+    G.check_out(G.host_f64(out[torch.from_numpy(tok).cuda()]), ref["out"])
+    if fuse == 1:
+        assert torch.equal(out.view(torch.int16), dev.forward().view(torch.int16))
