@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import fine_grained_moe_02_b300 as moe
 import moe_inputs as mi
 from oracle import moe_oracle as O
 from tests import gpu_util as G
@@ -52,7 +53,6 @@ def test_full_clip_fused_forward_sampled(fuse):
     dev = G.Dev(inp)
     idx, _, _ = dev.route(want_logits=False)
     out = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.bfloat16, device="cuda")
-    import fine_grained_moe_02_b300 as moe
     moe.moe_forward_fused(dev.dims, dev.x, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, out, fuse, dev.ws)
     assert dev.status() == 0
     tok = mi.sample_tokens(cfg.T, 128, seed=23 + fuse)
