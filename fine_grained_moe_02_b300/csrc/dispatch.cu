@@ -20,14 +20,9 @@
 
 #include "internal.h"
 #include "moe.h"
+#include "ptx.cuh"
 
 namespace moe {
-
-// Programmatic dependent launch: wait for the preceding grid (a no-op when
-// this grid was launched without the attribute), and let the next grid be
-// scheduled once every block of this one has reached this point.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 constexpr int kTokBlock = 2048;   // tokens per hist/assign block
 constexpr int kAssignWarps = 16;  // warps per assign block; each owns kTokBlock/16 tokens
@@ -53,8 +48,8 @@ __device__ __forceinline__ void load_slots(const int32_t* __restrict__ row, int 
 __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int k,
                                                             int E, int32_t* __restrict__ block_counts,
                                                             int* status) {
-  pdl_wait();
-  pdl_trigger();
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   // head blockIdx.y of a batch of independent sorts
   topk_idx += static_cast<int64_t>(blockIdx.y) * T * k;
   block_counts += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
@@ -81,8 +76,8 @@ __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __res
 __global__ void __launch_bounds__(kAssignWarps * 32) dispatch_assign_kernel(
     const int32_t* __restrict__ topk_idx, int64_t T, int k, int E, const int32_t* __restrict__ block_counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ src_token) {
-  pdl_wait();
-  pdl_trigger();
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   // head blockIdx.y of a batch of independent sorts
   topk_idx += static_cast<int64_t>(blockIdx.y) * T * k;
   block_counts += static_cast<int64_t>(blockIdx.y) * gridDim.x * E;
@@ -212,8 +207,8 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
                                                               int64_t x_ld_vec, int64_t x_head_vec, int heads, int k,
                                                               const int32_t* __restrict__ row_of, int64_t rows,
                                                               uint4* __restrict__ x_perm) {
-  pdl_wait();
-  pdl_trigger();
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -245,31 +240,13 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(const uint4* __res
   }
 }
 
-// Launches `kern` with programmatic stream serialization: it may be scheduled
-// while the previous kernel on the stream is still running (it waits for it
-// with griddepcontrol.wait).
-template <class... P, class... A>
-cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, cudaStream_t stream, A... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
-}
-
 int launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
   const int nblk = static_cast<int>((a.T + kTokBlock - 1) / kTokBlock);
   const int heads = a.heads > 1 ? a.heads : 1;
-  if (launch_pdl(dispatch_hist_kernel, dim3(nblk, heads), dim3(256), stream, a.topk_idx, a.T, a.k, a.E,
+  if (launch_pdl(dispatch_hist_kernel, dim3(nblk, heads), dim3(256), 0, stream, a.topk_idx, a.T, a.k, a.E,
                  a.block_counts, a.status) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_pdl(dispatch_assign_kernel, dim3(nblk, heads), dim3(kAssignWarps * 32), stream, a.topk_idx, a.T, a.k,
+  if (launch_pdl(dispatch_assign_kernel, dim3(nblk, heads), dim3(kAssignWarps * 32), 0, stream, a.topk_idx, a.T, a.k,
                  a.E, a.block_counts, a.offsets, a.row_of, a.src_token) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (a.x_perm != nullptr) {
@@ -277,7 +254,7 @@ int launch_dispatch(const DispatchArgs& a, cudaStream_t stream) {
     const int64_t want = (a.T * heads + 7) / 8;  // 8 warps (tokens) per CTA
     const int grid = static_cast<int>(want < a.sm_count * 8LL ? want : a.sm_count * 8LL);
     const int64_t x_ld_vec = (a.x_ld ? a.x_ld : a.d) / 8;
-    if (launch_pdl(dispatch_gather_kernel, dim3(grid), dim3(256), stream, reinterpret_cast<const uint4*>(a.x), a.T,
+    if (launch_pdl(dispatch_gather_kernel, dim3(grid), dim3(256), 0, stream, reinterpret_cast<const uint4*>(a.x), a.T,
                    d_vec, x_ld_vec, a.x_head_off / 8, heads, a.k, a.row_of, a.T * a.k,
                    reinterpret_cast<uint4*>(a.x_perm)) != cudaSuccess)
       return MOE_ERR_CUDA;

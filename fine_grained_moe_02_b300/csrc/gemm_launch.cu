@@ -56,6 +56,8 @@ int run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td
   static std::atomic<uint64_t> smem_set{0};
   if (!smem_attr_ready(kern, S::kDynBytes, smem_set)) return MOE_ERR_CUDA;
   if (grid < 1) grid = 1;
+  // a plain launch: chaining the GEMMs and the combine by programmatic
+  // dependent launch measured 3% slower on the clip workload
   kern<<<grid, kThreads, S::kDynBytes, stream>>>(ta, tb, td, shape, ep);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

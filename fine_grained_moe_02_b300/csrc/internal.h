@@ -27,6 +27,25 @@ inline bool smem_attr_ready(Kern kern, int bytes, std::atomic<uint64_t>& done) {
   return true;
 }
 
+// Launches `kern` with programmatic stream serialization: the grid may be
+// scheduled while the previous kernel on the stream is still running, and
+// waits for it with griddepcontrol.wait before it touches that kernel's data.
+template <class... P, class... A>
+inline cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+}
+
 struct DispatchArgs {
   const uint16_t* x;
   const int32_t* topk_idx;
