@@ -458,17 +458,21 @@ def main():
     # run: on this power-capped part the clocks settle over the first few
     # hundred ms of sustained load, and the timed region should see the
     # steady state, not the transient
-    extra_warm = 0
-    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    w0.record(stream)
-    while True:
-        for _ in range(5):
-            moe.moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws)
-        extra_warm += 5
-        w1.record(stream)
-        w1.synchronize()
-        if w0.elapsed_time(w1) >= 1000.0 * WARMUP_S or extra_warm >= 2000:
-            break
+    def settle(seconds):
+        """Untimed moe_forward calls until `seconds` of layer work have run; returns the call count."""
+        n = 0
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        while True:
+            for _ in range(5):
+                moe.moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws)
+            n += 5
+            w1.record(stream)
+            w1.synchronize()
+            if w0.elapsed_time(w1) >= 1000.0 * seconds or n >= 2000:
+                return n
+
+    extra_warm = settle(WARMUP_S)
     status = moe.moe_get_device_status(ws)
     if status != 0:
         raise SystemExit(f"device status {status:#x} after warm-up")
@@ -479,6 +483,8 @@ def main():
     vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     clocks = Clocks(vis[local] if local < len(vis) else local)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     clocks.start()
     t_start.record(stream)
@@ -486,26 +492,28 @@ def main():
         moe.moe_forward(dims, x, w_lat, w_head, bias, w13, w_down, out, ws)
     t_end.record(stream)
     barrier()
-    clk = clocks.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
-    if moe.moe_get_device_status(ws) != 0:
-        raise SystemExit("device status set during the timed region")
-
     # stage breakdown: the same sequence as separate calls with an event
-    # between stages, K steps right after (still under the same power cap)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    # between stages, K steps started right after the timed loop (no idle
+    # gap beyond one launch: an idle GPU drops its clocks, or recovers power
+    # budget, within a few hundred ms), the clock sampler still running
     s0.record(stream)
     for i in range(args.steps):
         step(evs[i])
     s1.record(stream)
     barrier()
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, "cuda")
+    if moe.moe_get_device_status(ws) != 0:
+        raise SystemExit("device status set during the timed region")
     staged_ms = s0.elapsed_time(s1) / args.steps
     stage_names = ["route", "dispatch", "gemm1", "gemm2", "combine"]
     stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(stage_names)}
     if moe.moe_get_device_status(ws) != 0:
         raise SystemExit("device status set during the stage loop")
+
+    # the variants below are compared in the same sustained state (the clock
+    # sampler's stop left the GPU idle for a moment)
+    settle(0.5)
 
     # the folded-router variant of the layer (moe_forward_folded), same workload
     w_router = torch.empty((E, 2 * d), dtype=torch.bfloat16, device="cuda")
@@ -647,8 +655,9 @@ def main():
                                   f"calls (>= {WARMUP_S:.1f} s of layer work) so the clocks reach their sustained "
                                   f"state before the timed region"},
         "stages_ms": stage_ms,
-        "stages_note": "CUDA events between the stages of the same sequence run as separate calls, the K steps "
-                       "right after the timed moe_forward loop",
+        "stages_note": "CUDA events between the stages of the same sequence run as separate calls, K steps queued "
+                       "right behind the timed moe_forward loop (where the host issues calls slower than the GPU "
+                       "runs them, as on the smallest workloads, stage times include the host's gaps)",
         "staged_step_ms": staged_ms,
         "grouped_gemm_tflops": gg_tf,
         "grouped_gemm_frac_bf16_peak": gg_tf / pk["bf16_sus"],
