@@ -175,31 +175,21 @@ int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w
     const int blocks = static_cast<int>((n + 255) / 256 < sms ? (n + 255) / 256 : sms);
     concat_offsets_kernel<<<blocks, 256, 0, s>>>(da.offsets, H, E, Tk, goff);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    if (fused) {  // both expert layers in one kernel, act never leaves the SM
-      fa.offsets = goff;
-      fa.rows = static_cast<int64_t>(H) * Tk;
-      fa.E = H * E;
-      fa.x_perm = da.x_perm;
-      fa.w13 = w13;
-      fa.w_down = w_down;
-      fa.y_perm = da.x_perm;  // each tile reads its x rows before it writes their y rows
-      fa.tiles = at<int32_t>(ws, l.tiles);
-      if ((rc = launch_ffn_fused(fa, s)) != MOE_OK) return rc;
-    }
-  }
-  if (fused) {
-  } else if (static_cast<int64_t>(H) * E <= kMaxGemmGroups) {
-    int32_t* goff = at<int32_t>(ws, l.goff);
     fa.offsets = goff;
     fa.rows = static_cast<int64_t>(H) * Tk;
     fa.E = H * E;
     fa.x_perm = da.x_perm;
     fa.w13 = w13;
-    fa.act = act;
-    if ((rc = launch_gemm1(fa, s)) != MOE_OK) return rc;
     fa.w_down = w_down;
-    fa.y_perm = da.x_perm;
-    if ((rc = launch_gemm2(fa, s)) != MOE_OK) return rc;
+    fa.y_perm = da.x_perm;  // each tile reads its x rows before it writes their y rows
+    if (fused) {            // both expert layers in one kernel, act never leaves the SM
+      fa.tiles = at<int32_t>(ws, l.tiles);
+      if ((rc = launch_ffn_fused(fa, s)) != MOE_OK) return rc;
+    } else {
+      fa.act = act;
+      if ((rc = launch_gemm1(fa, s)) != MOE_OK) return rc;
+      if ((rc = launch_gemm2(fa, s)) != MOE_OK) return rc;
+    }
   } else {
     for (int j = 0; j < H; ++j) {
       fa.offsets = da.offsets + static_cast<int64_t>(j) * (E + 1);

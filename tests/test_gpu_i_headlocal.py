@@ -102,6 +102,11 @@ def test_headlocal_per_head_router_bias():
     dict(T=129, d=768, n_heads=3, head_dim=256, E=256, inter=64, top_k=8),
     dict(T=700, d=768, n_heads=3, head_dim=256, E=40, inter=512, top_k=6),
     dict(T=200, d=1024, n_heads=16, head_dim=64, E=256, inter=64, top_k=2),   # 4096 experts: staged head by head
+    dict(T=900, d=256, n_heads=4, head_dim=64, E=16, inter=256, top_k=3),      # fused, 64-wide heads
+    dict(T=640, d=384, n_heads=2, head_dim=192, E=24, inter=384, top_k=4),     # fused, 3 k-slices, 3 pieces
+    dict(T=40, d=512, n_heads=2, head_dim=256, E=256, inter=128, top_k=2),     # fused, most groups empty
+    dict(T=2500, d=512, n_heads=2, head_dim=256, E=4, inter=256, top_k=1),     # fused, groups of many tiles
+    dict(T=300, d=1024, n_heads=16, head_dim=64, E=256, inter=128, top_k=2),   # fused over 4096 groups
 ])
 def test_fused_expert_kernel_gives_the_staged_bits(kw):
     # the fused expert kernel rounds act to bf16 exactly where the separate
