@@ -79,10 +79,11 @@ struct GemmShape {
 
 // Gather warps: the A operand's rows are fetched by 32*GW threads with 16-byte
 // cp.async copies, 8 lanes per 128-byte row slice (4 whole rows per warp
-// instruction); a thread signals a stage kGatherLag k-slices after issuing it,
-// once its own copies have landed (cp.async.wait_group) and a proxy fence has
-// ordered them before the tensor core's reads.
-constexpr int kGatherLag = 2;
+// instruction); each thread hands the stage's full barrier an arrival that
+// fires when its copies have landed (cp.async.mbarrier.arrive.noinc) and goes
+// on to the next stage at once.  The MMA thread, having seen the barrier
+// complete, orders those generic-proxy writes before the tensor core's
+// async-proxy reads with a proxy fence of its own.
 
 template <int BN>
 struct GemmSmem {
@@ -184,7 +185,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
   __shared__ int s_bad;
 
   static_assert(kBM % (4 * (GW > 0 ? GW : 1)) == 0, "gather warps cover the tile's rows evenly");
-  static_assert(kGatherLag < STAGES, "a gather thread must be able to issue past the stage it signals");
+  static_assert(GW % 2 == 0, "a gather thread's rows r, r + 4*GW, ... share one 128-byte swizzle phase");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = shape.N / BN;
@@ -279,7 +280,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const uint64_t pol = ptx::policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
-    int64_t issued = 0;
     bool ok = true;
     for (int tile = first_tile; tile < total && ok; tile += tile_step) {
       const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
@@ -305,13 +305,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
         for (int j = 0; j < kRowsPer; ++j)  // row r_first + j*kRowStep keeps the swizzle of r_first (kRowStep % 8 == 0)
           ptx::cp_async_16(sa + static_cast<uint32_t>(j * kRowStep) * 128u, src[j] + kb * kBK,
                            ((valid >> j) & 1u) ? 16u : 0u, pol);
-        ptx::cp_async_commit();
-        if (issued >= kGatherLag) {
-          ptx::cp_async_wait<kGatherLag>();
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(ptx::smem_u32(&full_bar[(issued - kGatherLag) % STAGES]));
-        }
-        ++issued;
+        ptx::cp_async_mbar_arrive_noinc(ptx::smem_u32(&full_bar[stage]));
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
     }
@@ -319,11 +313,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       atomicOr(shape.status, MOE_DEV_TIMEOUT);
       s_abort = 1;
     }
-    // drain: this thread's copies land, and its last stages are signaled
-    ptx::cp_async_wait<0>();
-    ptx::fence_proxy_async_smem();
-    for (int64_t i = issued > kGatherLag ? issued - kGatherLag : 0; i < issued; ++i)
-      ptx::mbar_arrive(ptx::smem_u32(&full_bar[i % STAGES]));
+    // drain: this thread's copies land before it may exit (their barrier
+    // arrivals are awaited by the producer's drain)
+    ptx::cp_async_wait_all();
   } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -396,6 +388,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
             break;
           }
           ptx::tc_fence_after();
+          if (GW > 0) ptx::fence_proxy_async_smem();  // the gathered A rows were written by cp.async
           const uint32_t sa = ptx::smem_u32(smem + stage * S::kStageBytes);
           const uint32_t sb = sa + S::kABytes;
 #pragma unroll

@@ -264,14 +264,13 @@ int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t
 /* moe_expert_gemm1 with the sorting gather fused into the operand loads:
  * row r of the A operand is x[src_token[r]] (x [T, d], src_token from
  * moe_dispatch / moe_dispatch_indices), fetched with 16-byte asynchronous
- * copies by two extra warps of the GEMM kernel, so x_perm is never
+ * copies by four extra warps of the GEMM kernel, so x_perm is never
  * materialised (saves T*top_k*d*2 bytes of memory and the gather's HBM round
  * trip).  The result equals moe_expert_gemm1 on the gathered x_perm bit for
- * bit.  moe_forward_fused with MOE_FUSE_GATHER runs it; on B300 that layer
- * is ~1.7 ms slower on the clip workload than the separate gather plus
- * moe_expert_gemm1 (19.2 against 17.5 ms: the copies are handed to the
- * tensor core stage by stage, two k-slices behind), so moe_forward keeps
- * the separate gather. */
+ * bit.  moe_forward_fused with MOE_FUSE_GATHER runs it; on B300 the gathered
+ * GEMM-1 takes ~1.12x the time of moe_expert_gemm1 on x_perm, about what the
+ * separate gather costs, so that layer and moe_forward run at the same speed
+ * on the clip workload; moe_forward keeps the separate gather. */
 int moe_expert_gemm1_gather(const moe_dims* dims, const moe_bf16* x, const int32_t* src_token,
                             const int32_t* offsets, const moe_bf16* w13, moe_bf16* act, void* ws, size_t ws_bytes,
                             void* stream);
