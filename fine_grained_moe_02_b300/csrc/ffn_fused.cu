@@ -177,9 +177,14 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         }
         return true;
       };
+      // tiles are decoded once each, the next one while this one's first
+      // gate/up slices wait for ring slots (a decode is a binary search of
+      // dependent global loads; done at the top of each tile it delayed the
+      // tile's first loads)
+      int g = 0, row0 = 0, hi = 0;
+      if (static_cast<int>(blockIdx.x) < n_tiles) g = decode(blockIdx.x, &row0, &hi);
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tiles) {
-        int row0, hi;
-        const int g = decode(t, &row0, &hi);
+        int g_n = 0, row0_n = 0, hi_n = 0;
         {
           // the tile's x rows, once the previous tile's gate/up products are done with them
           if (!ptx::mbar_wait(ptx::smem_u32(&x_empty), (tiles & 1) ^ 1, &s_abort, a.wait_ns)) { ok = false; break; }
@@ -189,9 +194,11 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
           x_loaded = true;
           // ring order: w13(0), w13(1), wd(0), w13(2), wd(1), ..., w13(np-1), wd(np-2), wd(np-1)
           ok = push_w13(g, 0);
+          if (t + static_cast<int>(gridDim.x) < n_tiles) g_n = decode(t + gridDim.x, &row0_n, &hi_n);
           for (int p = 1; p < np && ok; ++p) ok = push_w13(g, p) && push_wd(g, p - 1);
           if (ok) ok = push_wd(g, np - 1);
         }
+        g = g_n, row0 = row0_n, hi = hi_n;
       }
       if (!ok) {
         atomicOr(a.status, MOE_DEV_TIMEOUT);
@@ -310,19 +317,22 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
           if (!wait(acc1_full, q & 1)) break;
           // this part's chunk: gate columns [128 part, +64), up columns [128 part + 64, +64)
           uint32_t pk[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float gv[32], uv[32];
+          {
+            uint32_t gr[64], ur[64];
             __syncwarp();
-            tmem_ld32(lane_addr + part * 128 + h * 32, gv);
-            tmem_ld32(lane_addr + part * 128 + 64 + h * 32, uv);
-            if (h == 1) {  // acc1 may take the next piece's products while this warp finishes
-              ptx::tc_fence_before();
-              ptx::mbar_arrive(ptx::smem_u32(&acc1_empty));
-            }
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[h * 16 + i] = pack_bf16x2(silu(gv[2 * i]) * uv[2 * i], silu(gv[2 * i + 1]) * uv[2 * i + 1]);
+            for (int c = 0; c < 4; ++c) {
+              ptx::tmem_ld16(lane_addr + part * 128 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(gr + 16 * c));
+              ptx::tmem_ld16(lane_addr + part * 128 + 64 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(ur + 16 * c));
+            }
+            ptx::tmem_ld_wait();  // one wait for all eight loads: acc1 is held for the loads alone
+            // acc1 may take the next piece's products while this warp finishes
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&acc1_empty));
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              pk[i] = pack_bf16x2(silu(__uint_as_float(gr[2 * i])) * __uint_as_float(ur[2 * i]),
+                                  silu(__uint_as_float(gr[2 * i + 1])) * __uint_as_float(ur[2 * i + 1]));
           }
           const int b = q & 1;
           if (!wait(act_free[b], ((q >> 1) & 1) ^ 1)) break;
