@@ -30,6 +30,7 @@ MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_TIMEOUT = 0x2
 MOE_DEV_BAD_OFFSETS = 0x4
 MOE_DEV_BAD_MODALITY = 0x8
+MOE_DEV_BAD_SOURCE_ROW = 0x10
 MOE_FUSE_GATHER = 0x1
 MOE_FUSE_GATE = 0x2
 

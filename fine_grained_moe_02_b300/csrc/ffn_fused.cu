@@ -7,8 +7,10 @@
 // for the head-local experts of that section (one 256-dim head slice in and
 // out).
 //
-// Per tile (128 rows of one expert group; its x rows stay in shared memory
-// for the whole tile) and per 128-column piece p of the intermediate:
+// Per tile (128 rows of one expert group; its x rows, the head slices of the
+// group's tokens, are copied from x by source token into shared memory and
+// stay there for the whole tile) and per 128-column piece p of the
+// intermediate:
 //   1. acc1 = x W13[256p, 256p + 256)^T   (gate | up of chunk 2p, gate | up of
 //      chunk 2p+1: 64 columns each, TMEM)
 //   2. act_p = bf16(silu(gate) * up)       (epilogue -> shared memory, two
@@ -29,13 +31,16 @@
 // neighbouring CTAs at the same time and read its weights from DRAM once,
 // the rest from L2.  (One CTA taking every block of a group in turn read
 // each group's weights once per block: 148 groups' weights in flight do not
-// stay in L2 between blocks.)  Roles (320 threads, one CTA per SM):
-// warp 0 lane 0 loads with TMA (the tile's x rows; then w13 and W_down
-// slices through a ring in the MMA thread's order), warp 1 lane 0 issues
-// tcgen05.mma, warps 2..9 run SwiGLU and store y (warps w and w + 4 share
-// TMEM lane quadrant w % 4; the first takes chunk 2p and the first half of
-// y's columns, the second chunk 2p+1 and the rest).  Every wait is bounded
-// as in the GEMM engine.
+// stay in L2 between blocks.)  Roles (384 threads, one CTA per SM):
+// warp 0 lane 0 loads w13 and W_down slices with TMA through a ring in the
+// MMA thread's order, warp 1 lane 0 issues tcgen05.mma, warps 2..9 run
+// SwiGLU and store y (warps w and w + 4 share TMEM lane quadrant w % 4; the
+// first takes chunk 2p and the first half of y's columns, the second chunk
+// 2p+1 and the rest), warps 10..11 gather the next tile's x rows with
+// cp.async as soon as the gate/up products are done with the current ones
+// (x is read from L2, 66 MB for the 10,752-token head-local workload, so
+// the sorted copy x_perm never exists).  Every wait is bounded as in the
+// GEMM engine.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -60,13 +65,23 @@ constexpr int kFActBytes = 2 * kFSub;           // one piece of act: two 64-colu
 constexpr int kFDynBytes = kFXBytes + kFStages * kFStageBytes + 2 * kFActBytes + 1024;
 constexpr uint32_t kAcc2Col = 256;              // TMEM column of the down-projection accumulator
 constexpr int kFEpiWarps = 8;
-constexpr int kFThreads = 64 + 32 * kFEpiWarps;
+constexpr int kFGatherWarp = 2 + kFEpiWarps;  // the first warp after the epilogue warps
+constexpr int kFGatherWarps = 2;
+constexpr int kFThreads = 32 * (kFGatherWarp + kFGatherWarps);
+constexpr int kFGatherRows = kBM / kFGatherWarps;  // tile rows per gather warp
 
 struct FfnFusedArgs {
   const int* offsets;  // [groups + 1] group row offsets
   const int* tiles;    // [groups + 1] exclusive prefix of the groups' 128-row tile counts
   int groups;
-  int rows;            // rows of x_perm / y_perm
+  int rows;            // rows of y (the sorted rows of all groups)
+  // Row r of a tile of group g is x[src[r], (g / head_groups) * D + (0 .. D)):
+  // x is [T, x_ld] bf16, src [rows] token indices
+  const uint16_t* x;
+  int64_t x_ld;
+  const int* src;
+  int T;
+  int head_groups;
   int D, I;
   uint16_t* y;         // [rows, D]
   int* status;
@@ -74,8 +89,8 @@ struct FfnFusedArgs {
 };
 
 __global__ void __launch_bounds__(kFThreads, 1)
-ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w13,
-                 const __grid_constant__ CUtensorMap tmap_wd, FfnFusedArgs a) {
+ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_w13, const __grid_constant__ CUtensorMap tmap_wd,
+                 FfnFusedArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xs = smem;                               // [D / 64][128 rows x 64]
@@ -100,7 +115,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       ptx::mbar_init(ptx::smem_u32(&full_bar[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&empty_bar[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&x_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&x_full), 32 * kFGatherWarps);  // every gather lane, once its copies land
     ptx::mbar_init(ptx::smem_u32(&x_empty), 1);
     ptx::mbar_init(ptx::smem_u32(&acc1_full), 1);
     ptx::mbar_init(ptx::smem_u32(&acc1_empty), kEpiThreads);
@@ -118,7 +133,6 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
     ptx::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tmap_x);
     ptx::prefetch_tmap(&tmap_w13);
     ptx::prefetch_tmap(&tmap_wd);
   }
@@ -147,8 +161,8 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       // ------------------------------------------------------------ producer
       const uint64_t pol = ptx::policy_evict_last();
       int stage = 0;
-      uint32_t phase = 0, filled = 0, last_par = 0, tiles = 0;
-      bool ok = true, x_loaded = false;
+      uint32_t phase = 0, filled = 0, last_par = 0;
+      bool ok = true;
       auto next_slot = [&](uint32_t bytes) -> uint32_t {
         if (!ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, a.wait_ns)) return 0;
         ptx::mbar_arrive_expect_tx(ptx::smem_u32(&full_bar[stage]), bytes);
@@ -181,24 +195,18 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       // gate/up slices wait for ring slots (a decode is a binary search of
       // dependent global loads; done at the top of each tile it delayed the
       // tile's first loads)
-      int g = 0, row0 = 0, hi = 0;
-      if (static_cast<int>(blockIdx.x) < n_tiles) g = decode(blockIdx.x, &row0, &hi);
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tiles) {
-        int g_n = 0, row0_n = 0, hi_n = 0;
+      int g = 0, r0, r1;
+      if (static_cast<int>(blockIdx.x) < n_tiles) g = decode(blockIdx.x, &r0, &r1);
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        int g_n = 0;
         {
-          // the tile's x rows, once the previous tile's gate/up products are done with them
-          if (!ptx::mbar_wait(ptx::smem_u32(&x_empty), (tiles & 1) ^ 1, &s_abort, a.wait_ns)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(ptx::smem_u32(&x_full), static_cast<uint32_t>(ksub * kFSub));
-          for (int kb = 0; kb < ksub; ++kb)
-            ptx::tma_load_2d(ptx::smem_u32(xs + kb * kFSub), &tmap_x, kb * kBK, row0, ptx::smem_u32(&x_full), pol);
-          x_loaded = true;
           // ring order: w13(0), w13(1), wd(0), w13(2), wd(1), ..., w13(np-1), wd(np-2), wd(np-1)
           ok = push_w13(g, 0);
-          if (t + static_cast<int>(gridDim.x) < n_tiles) g_n = decode(t + gridDim.x, &row0_n, &hi_n);
+          if (t + static_cast<int>(gridDim.x) < n_tiles) g_n = decode(t + gridDim.x, &r0, &r1);
           for (int p = 1; p < np && ok; ++p) ok = push_w13(g, p) && push_wd(g, p - 1);
           if (ok) ok = push_wd(g, np - 1);
         }
-        g = g_n, row0 = row0_n, hi = hi_n;
+        g = g_n;
       }
       if (!ok) {
         atomicOr(a.status, MOE_DEV_TIMEOUT);
@@ -210,8 +218,6 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         if ((filled & (1u << s)) &&
             !ptx::mbar_wait(ptx::smem_u32(&full_bar[s]), (last_par >> s) & 1u, &never, a.wait_ns))
           atomicOr(a.status, MOE_DEV_TIMEOUT);
-      if (x_loaded && !ptx::mbar_wait(ptx::smem_u32(&x_full), (tiles - 1) & 1u, &never, a.wait_ns))
-        atomicOr(a.status, MOE_DEV_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -269,6 +275,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
         {
           if (!wait(x_full, tiles & 1)) break;
+          ptx::fence_proxy_async_smem();  // the x rows were written by the gather warp's cp.async
           if (!mma1(np == 1)) break;
           for (int p = 1; p < np && ok; ++p) {
             // order: gate/up(p-1), down(p-2), gate/up(p), down(p-1): the
@@ -290,7 +297,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
       const volatile int never = 0;
       if (!ptx::mbar_wait(ptx::smem_u32(&drain_bar), 0, &never, a.wait_ns)) atomicOr(a.status, MOE_DEV_TIMEOUT);
     }
-  } else {
+  } else if (warp < kFGatherWarp) {
     // -------------------------------------------------------------- epilogue
     const int quad = warp & 3;
     const int part = (warp - 2) / 4;  // 0: chunk 2p, first half of y; 1: chunk 2p+1, second half
@@ -369,6 +376,65 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_consta
         }
       }
     }
+  } else {
+    // ---------------------------------------------------------------- gather
+    // Each tile's x rows, head slice of x by source token, straight into the
+    // 128-byte-swizzled sub-tiles the MMA descriptors expect: 8 lanes per
+    // 128-byte row slice, 4 rows per warp instruction.  Each lane's arrival
+    // on x_full fires once its copies have landed; the MMA thread fences the
+    // async proxy after that barrier.  x is read from L2 (each token's head
+    // slice is read by its top-k experts), x_perm never exists.
+    const uint64_t pol = ptx::policy_evict_last();
+    const int chunk = lane & 7, rsub = lane >> 3;
+    const int rbase = (warp - kFGatherWarp) * kFGatherRows;  // this warp's first tile row
+    uint32_t tiles = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tiles) {
+      int row0, hi;
+      const int g = decode(t, &row0, &hi);
+      const int64_t col0 = static_cast<int64_t>(g / a.head_groups) * a.D + chunk * 8;
+      // this warp's source tokens, one per lane per 32 rows in one coalesced
+      // pass (-1: past the group's rows, or out of range and flagged)
+      int toks[kFGatherRows / 32];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < kFGatherRows / 32; ++i) {
+        const int row = row0 + rbase + 32 * i + lane;
+        int tok = row < hi ? __ldg(a.src + row) : -1;
+        if (row < hi && (tok < 0 || tok >= a.T)) {
+          bad = true;
+          tok = -1;
+        }
+        toks[i] = tok;
+      }
+      if (bad) atomicOr(a.status, MOE_DEV_BAD_SOURCE_ROW);
+      // (the decode and the token loads above do not need x free); the
+      // previous tile's gate/up products are done with the x sub-tiles
+      const bool got = ptx::mbar_wait(ptx::smem_u32(&x_empty), (tiles & 1) ^ 1, &s_abort, a.wait_ns);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) atomicOr(a.status, MOE_DEV_TIMEOUT);
+        s_abort = 1;
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int j = 0; j < kFGatherRows / 4; ++j) {
+        const int r = rbase + 4 * j + rsub;  // r - rbase = 32 * (j / 8) + (4 * (j % 8) + rsub)
+        const int tok = __shfl_sync(0xffffffffu, toks[j / 8], 4 * (j % 8) + rsub);
+        const bool v = tok >= 0;
+        const uint16_t* src = a.x + static_cast<int64_t>(v ? tok : 0) * a.x_ld + col0;
+        const uint32_t dst = ptx::smem_u32(xs) + static_cast<uint32_t>(r) * 128u +
+                             ((static_cast<uint32_t>(chunk) ^ (static_cast<uint32_t>(r) & 7u)) << 4);
+        for (int kb = 0; kb < ksub; ++kb)
+          ptx::cp_async_16(dst + static_cast<uint32_t>(kb * kFSub), src + kb * kBK, v ? 16u : 0u, pol);
+      }
+      ptx::cp_async_mbar_arrive_noinc(ptx::smem_u32(&x_full));
+    }
+    // drain: this lane's copies land, and their barrier arrival with them
+    ptx::cp_async_wait_all();
+    const volatile int never = 0;
+    if (tiles > 0 && !ptx::mbar_wait(ptx::smem_u32(&x_full), (tiles - 1) & 1u, &never, a.wait_ns))
+      atomicOr(a.status, MOE_DEV_TIMEOUT);
   }
 
   ptx::tc_fence_before();
@@ -434,9 +500,10 @@ bool ffn_fused_supported(int D, int I) { return D % 64 == 0 && D >= 64 && D <= k
 
 int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream) {
   if (!ffn_fused_supported(a.d, a.I)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (a.rows >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  CUtensorMap tx, tw, td;
-  if (!make_tmap_bf16_2d(&tx, a.x_perm, a.d, a.rows, kBK, kBM)) return MOE_ERR_CUDA;
+  if (a.rows >= (int64_t{1} << 31) || a.T >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a.x == nullptr || a.src_token == nullptr || a.head_groups < 1 || a.x_ld < a.d || a.x_ld % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  CUtensorMap tw, td;
   if (!make_tmap_bf16_2d(&tw, a.w13, a.d, static_cast<uint64_t>(a.E) * 2 * a.I, kBK, 256)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&td, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, a.d)) return MOE_ERR_CUDA;
   if (a.tiles == nullptr || a.E < 1) return MOE_ERR_INVALID_ARG;
@@ -447,6 +514,11 @@ int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream) {
   fa.tiles = a.tiles;
   fa.groups = a.E;
   fa.rows = static_cast<int>(a.rows);
+  fa.x = a.x;
+  fa.x_ld = a.x_ld;
+  fa.src = a.src_token;
+  fa.T = static_cast<int>(a.T);
+  fa.head_groups = a.head_groups;
   fa.D = a.d;
   fa.I = a.I;
   fa.y = a.y_perm;
@@ -455,7 +527,7 @@ int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   if (!smem_attr_ready(ffn_fused_kernel, kFDynBytes, smem_set)) return MOE_ERR_CUDA;
   // at most one CTA per SM; a CTA with no tile returns at once
-  ffn_fused_kernel<<<a.sm_count, kFThreads, kFDynBytes, stream>>>(tx, tw, td, fa);
+  ffn_fused_kernel<<<a.sm_count, kFThreads, kFDynBytes, stream>>>(tw, td, fa);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -208,6 +208,7 @@ int launch_gemm1_gather(const FfnArgs& a, cudaStream_t stream) {
   GemmShape sh{a.d, a.d, n, a.E, a.offsets, rows, a.status, a.src_token};
   sh.a_src = a.x;
   sh.a_ld = a.d;
+  sh.a_src_rows = static_cast<int>(a.T);
   EpiSwiGLU::Params ep{a.act, a.I};
   return (bn == 256) ? run_gemm<256, EpiSwiGLU, kGatherWarps>(tb, tb, td, sh, ep, a.sm_count, stream, bn)
                      : run_gemm<128, EpiSwiGLU, kGatherWarps>(tb, tb, td, sh, ep, a.sm_count, stream, bn);

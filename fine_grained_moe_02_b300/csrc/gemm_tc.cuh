@@ -75,6 +75,7 @@ struct GemmShape {
   int b_group_rows;
   const uint16_t* a_src;
   int64_t a_ld;
+  int a_src_rows;   // rows of a_src: a gathered index outside [0, a_src_rows) reads zeros
 };
 
 // Gather warps: the A operand's rows are fetched by 32*GW threads with 16-byte
@@ -285,14 +286,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
       const uint16_t* src[kRowsPer];
       uint32_t valid = 0;
+      bool bad_row = false;
 #pragma unroll
       for (int j = 0; j < kRowsPer; ++j) {
         const int row = c.row0 + r_first + j * kRowStep;
-        const bool v = row < c.row_end;
-        const int tok = v ? __ldg(shape.a_gather + row) : 0;
+        int tok = row < c.row_end ? __ldg(shape.a_gather + row) : -1;
+        if (row < c.row_end && (tok < 0 || tok >= shape.a_src_rows)) bad_row = true;
+        const bool v = tok >= 0 && tok < shape.a_src_rows;
+        if (!v) tok = 0;
         src[j] = shape.a_src + static_cast<int64_t>(tok) * shape.a_ld + chunk * 8;
         valid |= (v ? 1u : 0u) << j;
       }
+      if (bad_row) atomicOr(shape.status, MOE_DEV_BAD_SOURCE_ROW);
       for (int kb = 0; kb < num_kb; ++kb) {
         bool got = true;
         if (lane == 0) got = ptx::mbar_wait(ptx::smem_u32(&empty_bar[stage]), phase ^ 1, &s_abort, wait_ns);

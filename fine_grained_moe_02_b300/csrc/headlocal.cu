@@ -153,7 +153,9 @@ int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w
   da.offsets = at<int32_t>(ws, l.offsets);
   da.row_of = at<int32_t>(ws, l.row_of);
   da.src_token = at<int32_t>(ws, l.src);
-  da.x_perm = at<uint16_t>(ws, l.xperm);
+  const bool fused = !staged && ffn_fused_supported(Dh, I);
+  // the fused expert kernel gathers its x rows itself: the sort is indices only
+  da.x_perm = fused ? nullptr : at<uint16_t>(ws, l.xperm);
   da.block_counts = at<int32_t>(ws, l.disp);
   da.status = status;
   da.sm_count = sms;
@@ -168,7 +170,6 @@ int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w
   fa.status = status;
   fa.sm_count = sms;
   uint16_t* act = at<uint16_t>(ws, l.act);
-  const bool fused = !staged && ffn_fused_supported(Dh, I);
   if (fused || static_cast<int64_t>(H) * E <= kMaxGemmGroups) {
     int32_t* goff = at<int32_t>(ws, l.goff);
     const int64_t n = static_cast<int64_t>(H) * E + 1;
@@ -181,8 +182,13 @@ int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w
     fa.x_perm = da.x_perm;
     fa.w13 = w13;
     fa.w_down = w_down;
-    fa.y_perm = da.x_perm;  // each tile reads its x rows before it writes their y rows
-    if (fused) {            // both expert layers in one kernel, act never leaves the SM
+    fa.y_perm = at<uint16_t>(ws, l.xperm);  // x_perm's region (staged: x_perm is dead once GEMM-1 has read it)
+    if (fused) {  // both expert layers in one kernel, x gathered on chip, act never leaves the SM
+      fa.x = x;
+      fa.x_ld = dims->d;
+      fa.src_token = da.src_token;
+      fa.T = T;
+      fa.head_groups = E;
       fa.tiles = at<int32_t>(ws, l.tiles);
       if ((rc = launch_ffn_fused(fa, s)) != MOE_OK) return rc;
     } else {
@@ -207,7 +213,7 @@ int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w
 
   // 4. every head's combine into its columns of out, one launch
   CombineArgs ca{};
-  ca.y_perm = da.x_perm;
+  ca.y_perm = at<uint16_t>(ws, l.xperm);
   ca.row_of = da.row_of;
   ca.gate = gate;
   ca.out = out;

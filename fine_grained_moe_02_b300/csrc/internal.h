@@ -113,6 +113,10 @@ struct FfnArgs {
   const float* gate;         // [T, k]
   int k;
   int32_t* tiles;            // scratch [E + 1] (the fused expert kernel's tile table)
+  // fused expert kernel: row r of group g is x[src_token[r], (g / head_groups) * d + (0 .. d)),
+  // x with x_ld elements per row
+  int64_t x_ld;
+  int head_groups;
 };
 
 struct CombineArgs {

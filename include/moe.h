@@ -84,6 +84,7 @@ typedef enum moe_status {
 #define MOE_DEV_TIMEOUT 0x2        /* a pipeline wait exceeded its limit; that kernel stopped early */
 #define MOE_DEV_BAD_OFFSETS 0x4    /* group offsets not monotone / out of range; no tile was run */
 #define MOE_DEV_BAD_MODALITY 0x8   /* a token's modality id is outside [0, n_modalities); its routed slots are -1 */
+#define MOE_DEV_BAD_SOURCE_ROW 0x10 /* a gathered row's src_token entry is outside [0, T); the row was read as zeros */
 
 /* Human-readable name of a moe_status value.  Never NULL. */
 const char* moe_status_string(int status);
@@ -270,7 +271,9 @@ int moe_expert_gemm1(const moe_dims* dims, const moe_bf16* x_perm, const int32_t
  * bit.  moe_forward_fused with MOE_FUSE_GATHER runs it; on B300 the gathered
  * GEMM-1 takes ~1.12x the time of moe_expert_gemm1 on x_perm, about what the
  * separate gather costs, so that layer and moe_forward run at the same speed
- * on the clip workload; moe_forward keeps the separate gather. */
+ * on the clip workload; moe_forward keeps the separate gather.  A src_token
+ * entry outside [0, T) is not dereferenced: that row reads as zeros and
+ * MOE_DEV_BAD_SOURCE_ROW is set in the status word of `ws`. */
 int moe_expert_gemm1_gather(const moe_dims* dims, const moe_bf16* x, const int32_t* src_token,
                             const int32_t* offsets, const moe_bf16* w13, moe_bf16* act, void* ws, size_t ws_bytes,
                             void* stream);
@@ -395,15 +398,18 @@ int moe_forward_ext(const moe_dims* dims, const moe_ext* ext, const moe_bf16* x,
  *   topk_idx [n_heads, T, top_k] int32 or NULL (written: each head's choice)
  *   logits [n_heads, T, E] fp32 or NULL (written: each head's scores)
  * Rules: head_dim % 64 == 0, inter % 64 == 0, E <= 256, top_k <= min(8, E).
- * All heads' routers run as one batched GEMM, their sorts, gathers and
- * combines as single launches over (head, token), all on `stream`.  With
- * head_dim <= 256 both expert layers of all n_heads * E head-local experts
- * run as one fused kernel that keeps each 128-row tile's activations on chip
- * (the gate/up products in tensor memory, SwiGLU into shared memory, the
- * down projection accumulating in tensor memory): the act intermediate never
- * reaches HBM.  moe_forward_headlocal_staged runs the same layer with the two
- * expert layers as separate grouped GEMMs (act through the workspace; head
- * by head when n_heads * E > 3072); both give the same bits. */
+ * All heads' routers run as one batched GEMM, their sorts and combines as
+ * single launches over (head, token), all on `stream`.  With head_dim <= 256
+ * and inter a multiple of 128, both expert layers of all n_heads * E
+ * head-local experts run as one fused kernel: it copies each 128-row tile's
+ * x head slices from x by source token into shared memory (no sorted copy of
+ * x is written) and keeps the tile's activations on chip (the gate/up
+ * products in tensor memory, SwiGLU into shared memory, the down projection
+ * accumulating in tensor memory), so neither x_perm nor act reaches HBM.
+ * moe_forward_headlocal_staged runs the same layer with a separate gather
+ * and the two expert layers as separate grouped GEMMs (x_perm and act
+ * through the workspace; head by head when n_heads * E > 3072); both give
+ * the same bits. */
 int moe_workspace_size_headlocal(const moe_dims* dims, size_t* bytes);
 int moe_prepare_weights_headlocal(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
                                   void* stream);

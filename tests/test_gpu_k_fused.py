@@ -7,6 +7,7 @@ against the fp64 oracle:
 * expert GEMM-2 with the gate in its epilogue (moe_expert_gemm2_gated) and
   the unweighted row combine (moe_combine_rows);
 * moe_forward_fused with every choice of fusions, end to end;
+* a gathered row whose source index is outside x: read as zeros, flagged;
 * the SwiGLU epilogue's silu over the whole range it meets, element-wise,
   on inputs whose GEMM sums are exact in fp32.
 """
@@ -60,24 +61,27 @@ def _gathered_case(T, d, E, I, counts, seed, exact=False):
     return (R, offsets, src, mi.f32_to_bf16_bits(x), mi.f32_to_bf16_bits(wg), mi.f32_to_bf16_bits(wu))
 
 
-def _run_gemm1(T, d, E, I, offsets, src, x, wg, wu, gathered):
+def _run_gemm1(T, d, E, I, offsets, src, x, wg, wu, gathered, status=0):
+    """act of the R = offsets[-1] rows.  dims.T covers both x's T tokens and
+    the R rows (top_k = 1): x is [dims.T, d] and src_token indexes it."""
     R = int(offsets[-1])
-    dims = moe.moe_dims.make(max(R, 1), d, E, I, 1, n_heads=1, head_dim=256)
+    Td = max(T, R, 1)
+    dims = moe.moe_dims.make(Td, d, E, I, 1, n_heads=1, head_dim=256)
     ws = moe.alloc_workspace(moe.moe_scratch_size(dims))
     w13 = torch.empty((E, 2 * I, d), dtype=torch.bfloat16, device="cuda")
     moe.moe_prepare_weights(dims, G.dev_bf16(wg), G.dev_bf16(wu), w13)
-    act = torch.full((max(R, 1), I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    act = torch.full((Td, I), float("nan"), dtype=torch.bfloat16, device="cuda")
     off_d = torch.from_numpy(offsets).cuda()
     if gathered:
-        # the x buffer must hold `dims.T` rows for the binding's size check
-        xbuf = np.zeros((max(T, R, 1), d), np.uint16)
+        xbuf = np.zeros((Td, d), np.uint16)
         xbuf[:T] = x
-        src_d = torch.from_numpy(np.r_[src, np.zeros(max(R, 1) - R, np.int32)].astype(np.int32)).cuda()
+        src_d = torch.from_numpy(np.r_[src, np.zeros(Td - R, np.int32)].astype(np.int32)).cuda()
         moe.moe_expert_gemm1_gather(dims, G.dev_bf16(xbuf), src_d, off_d, w13, act, ws)
     else:
-        xp = x[src] if R else np.zeros((1, d), np.uint16)
+        xp = np.zeros((Td, d), np.uint16)
+        xp[:R] = x[src]
         moe.moe_expert_gemm1(dims, G.dev_bf16(xp), off_d, w13, act, ws)
-    assert moe.moe_get_device_status(ws) == 0
+    assert moe.moe_get_device_status(ws) == status
     return G.host_f64(act)[:R]
 
 
@@ -119,6 +123,22 @@ def test_gathered_gemm1_matches_oracle(T, d, E, I, counts):
     assert np.abs(act - ref).max() <= G.OUT_MAX_ABS
     # and the same bits as GEMM-1 on the gathered x_perm
     np.testing.assert_array_equal(act, _run_gemm1(T, d, E, I, offsets, src, x, wg, wu, gathered=False))
+
+
+def test_gathered_gemm1_reads_a_source_row_outside_x_as_zeros():
+    # a src_token entry outside [0, T) is never dereferenced: the row reads
+    # as zeros (act 0) and MOE_DEV_BAD_SOURCE_ROW is set; every other row is
+    # untouched
+    T, d, E, I = 300, 256, 2, 128
+    R, offsets, src, x, wg, wu = _gathered_case(T, d, E, I, [200, 77], seed=5)
+    good = _run_gemm1(T, d, E, I, offsets, src, x, wg, wu, gathered=True)
+    bad_src = src.copy()
+    bad_src[[5, 150, 276]] = [T + 1000, -3, 2 ** 31 - 1]
+    act = _run_gemm1(T, d, E, I, offsets, bad_src, x, wg, wu, gathered=True, status=B.MOE_DEV_BAD_SOURCE_ROW)
+    assert np.all(act[[5, 150, 276]] == 0)
+    keep = np.ones(R, bool)
+    keep[[5, 150, 276]] = False
+    np.testing.assert_array_equal(act[keep], good[keep])
 
 
 def test_gated_gemm2_and_row_combine_match_oracle():
