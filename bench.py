@@ -311,14 +311,14 @@ def measure_headlocal_variant(torch, moe, steps: int) -> dict:
         raise SystemExit("device status set by moe_forward_headlocal")
     ms = e0.elapsed_time(e1) / steps
     flops = cfg.T * cfg.n_heads * (2 * cfg.head_dim * cfg.E + 6 * cfg.top_k * cfg.head_dim * cfg.inter)
-    # the layer is bound by HBM: every head-local expert's weights are streamed
-    # once for few rows each, and x_perm, act and y_perm each go out and back
+    # every head-local expert's weights are streamed once for few rows each;
+    # the fused expert kernel gathers x's head slices on chip and keeps act
+    # there, so of the intermediates only y_perm goes out and back
     H, Dh, E, I, T = cfg.n_heads, cfg.head_dim, cfg.E, cfg.inter, cfg.T
     Tk = T * cfg.top_k
-    alg_bytes = (2 * T * cfg.d * 2 + H * E * Dh * 2          # x (router, gather), router weights
+    alg_bytes = (2 * T * cfg.d * 2 + H * E * Dh * 2          # x (router, expert gather), router weights
                  + H * Tk * 8                                 # indices + gates
                  + H * E * (2 * I * Dh + Dh * I) * 2          # expert weights
-                 + 2 * H * Tk * Dh * 2 + 2 * H * Tk * I * 2   # x_perm, act: written and read
                  + 2 * H * Tk * Dh * 2 + T * cfg.d * 2)       # y_perm written and read, out
     # the method's own bytes: x read once, router and expert weights, out written
     essential = T * cfg.d * 2 + H * E * Dh * 2 + H * E * (2 * I * Dh + Dh * I) * 2 + T * cfg.d * 2
@@ -330,9 +330,10 @@ def measure_headlocal_variant(torch, moe, steps: int) -> dict:
             "frac_hbm_note": "essential bytes (x, router and expert weights, out) over the layer time",
             "traffic_bytes": alg_bytes, "traffic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
             "traffic_frac": alg_bytes / (ms * 1e-3) / 1e9 / hbm,
-            "traffic_note": "bytes of this implementation incl. its x_perm, act and y_perm round trips",
-            "path": "moe_forward_headlocal: all heads' routers + top-k as one batched GEMM, one sort and gather "
-                    "over (head, token), grouped SwiGLU GEMMs head by head, one combine into each head's columns"}
+            "traffic_note": "bytes of this implementation incl. its y_perm round trip",
+            "path": "moe_forward_headlocal: all heads' routers + top-k as one batched GEMM, one sort over "
+                    "(head, token), one fused expert kernel over all heads' experts (x head slices gathered "
+                    "on chip, gate/up -> SwiGLU -> down with act on chip), one combine into each head's columns"}
 
 
 def measure_ext_variant(torch, moe, steps: int) -> dict:
