@@ -492,10 +492,26 @@ def moe_forward_host(dims, x_host, w_lat, w_head, bias, w13, w_down, out_host, w
 
 
 class MoeLayer:
-    """Device-resident weights plus a workspace; forward() runs moe_forward."""
+    """Device-resident weights plus a workspace; forward() runs the layer.
 
-    def __init__(self, dims: moe_dims, w_lat, w_head, bias, w_gate, w_up, w_down, device="cuda"):
+    router="latent" (default): moe_forward, the latent projection and head
+    scores as the pages define them.  router="folded": the router folded to
+    s = x (W_head W_lat)^T + b (moe_prepare_router once, then
+    moe_forward_folded; same outputs within the same tolerances).  fuse:
+    MOE_FUSE_GATHER and/or MOE_FUSE_GATE runs moe_forward_fused with those
+    fusions (latent router only)."""
+
+    def __init__(self, dims: moe_dims, w_lat, w_head, bias, w_gate, w_up, w_down, device="cuda",
+                 router: str = "latent", fuse: int = 0):
+        if router not in ("latent", "folded"):
+            raise ValueError(f"router must be 'latent' or 'folded', not {router!r}")
+        if fuse & ~(MOE_FUSE_GATHER | MOE_FUSE_GATE):
+            raise ValueError(f"unknown fusion bits {fuse:#x}")
+        if router == "folded" and fuse:
+            raise ValueError("the folded router runs the unfused layer (fuse=0)")
         self.dims = dims
+        self.router = router
+        self.fuse = fuse
         dev = torch.device(device)
         self.w_lat = w_lat.to(dev)
         self.w_head = w_head.to(dev)
@@ -505,12 +521,22 @@ class MoeLayer:
         self.w13 = torch.empty((dims.E, 2 * dims.inter, dims.d), dtype=torch.bfloat16, device=dev)
         moe_prepare_weights(dims, wg, wu, self.w13)
         del wg, wu
+        self.w_router = None
+        if router == "folded":
+            self.w_router = torch.empty((dims.E, 2 * dims.d), dtype=torch.bfloat16, device=dev)
+            moe_prepare_router(dims, self.w_lat, self.w_head, self.w_router)
         self.ws = alloc_workspace(moe_workspace_size(dims), dev)
 
     def forward(self, x, out=None, stream=None):
         if out is None:
             out = torch.empty((self.dims.T, self.dims.d), dtype=torch.bfloat16, device=x.device)
-        moe_forward(self.dims, x, self.w_lat, self.w_head, self.bias, self.w13, self.w_down, out, self.ws, stream)
+        if self.router == "folded":
+            moe_forward_folded(self.dims, x, self.w_router, self.bias, self.w13, self.w_down, out, self.ws, stream)
+        elif self.fuse:
+            moe_forward_fused(self.dims, x, self.w_lat, self.w_head, self.bias, self.w13, self.w_down, out,
+                              self.fuse, self.ws, stream)
+        else:
+            moe_forward(self.dims, x, self.w_lat, self.w_head, self.bias, self.w13, self.w_down, out, self.ws, stream)
         return out
 
     def device_status(self, stream=None) -> int:

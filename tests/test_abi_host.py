@@ -136,3 +136,12 @@ def test_undersized_tensors_are_rejected_before_any_device_work():
     with pytest.raises(ValueError, match="w_router"):
         moe.moe_forward_headlocal(h, bf(64 * 256), bf(2 * 8 * 128 - 1), None, bf(2 * 8 * 128 * 128),
                                   bf(2 * 8 * 128 * 64), bf(64 * 256), None, None, torch.zeros(1, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("kw", [dict(router="two_stage"), dict(fuse=4), dict(router="folded", fuse=1)])
+def test_layer_wrapper_rejects_unknown_options_before_any_device_work(kw):
+    import torch
+    dims = moe.moe_dims.make(256, 512, 16, 128, 6)
+    w = torch.empty(1, dtype=torch.bfloat16)   # never touched: the options are checked first
+    with pytest.raises(ValueError):
+        moe.MoeLayer(dims, w, w, None, w, w, w, device="cpu", **kw)

@@ -169,3 +169,26 @@ def test_forward_captured_in_a_cuda_graph_replays_with_new_inputs():
     assert dev.status() == 0
     assert torch.equal(out.view(torch.int16), ref2.view(torch.int16))
     assert not torch.equal(ref1.view(torch.int16), ref2.view(torch.int16))
+
+
+@pytest.mark.parametrize("router,fuse", [("latent", 0), ("folded", 0), ("latent", 1), ("latent", 3)])
+def test_layer_wrapper_runs_the_entry_point_it_names(router, fuse):
+    # MoeLayer(router=, fuse=) is plumbing only: its output has the bits of
+    # the entry point it selects (each of those is checked against the oracle
+    # in its own tests)
+    inp = mi.make_inputs("tiny")
+    cfg = inp["cfg"]
+    dev = G.Dev(inp)
+    layer = moe.MoeLayer(dev.dims, dev.w_lat, dev.w_head, dev.bias, G.dev_bf16(inp["w_gate"]),
+                         G.dev_bf16(inp["w_up"]), dev.w_down, router=router, fuse=fuse)
+    got = layer.forward(dev.x)
+    assert layer.device_status() == 0
+    want = torch.empty_like(got)
+    if router == "folded":
+        w = torch.empty((cfg.E, 2 * cfg.d), dtype=torch.bfloat16, device="cuda")
+        moe.moe_prepare_router(dev.dims, dev.w_lat, dev.w_head, w)
+        moe.moe_forward_folded(dev.dims, dev.x, w, dev.bias, dev.w13, dev.w_down, want, dev.ws)
+    else:
+        moe.moe_forward_fused(dev.dims, dev.x, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, want, fuse,
+                              dev.ws)
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
