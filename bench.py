@@ -283,10 +283,10 @@ def run_reference(args, rank, world):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def measure_headlocal_variant(torch, moe, steps: int) -> dict:
-    """moe_forward_headlocal on the headlocal workload (12 x 256 head slices,
-    256 experts per head, top-6 per head)."""
-    cfg = mi.CONFIGS["headlocal"]
+def measure_headlocal_variant(torch, moe, steps: int, name: str = "headlocal") -> dict:
+    """moe_forward_headlocal on a head-local workload (default: 12 x 256 head
+    slices, 256 experts per head, top-6 per head)."""
+    cfg = mi.CONFIGS[name]
     inp = mi.make_inputs(cfg)
 
     def up(u16):
@@ -393,8 +393,11 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     if args.variant is not None:  # one variant alone, on this rank's GPU
-        fn = measure_headlocal_variant if args.variant == "headlocal" else measure_ext_variant
-        line = fn(torch, moe, max(3, args.steps))
+        if args.variant == "headlocal":  # the head-local workload, or a head-local --workload given
+            name = args.workload if mi.CONFIGS[args.workload].head_local else "headlocal"
+            line = measure_headlocal_variant(torch, moe, max(3, args.steps), name)
+        else:
+            line = measure_ext_variant(torch, moe, max(3, args.steps))
         if rank == 0:
             print(json.dumps(line), flush=True)
         if world > 1:

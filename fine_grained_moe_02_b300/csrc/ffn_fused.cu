@@ -275,7 +275,6 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_w13, const __grid_cons
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
         {
           if (!wait(x_full, tiles & 1)) break;
-          ptx::fence_proxy_async_smem();  // the x rows were written by the gather warp's cp.async
           if (!mma1(np == 1)) break;
           for (int p = 1; p < np && ok; ++p) {
             // order: gate/up(p-1), down(p-2), gate/up(p), down(p-1): the
@@ -380,10 +379,12 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_w13, const __grid_cons
     // ---------------------------------------------------------------- gather
     // Each tile's x rows, head slice of x by source token, straight into the
     // 128-byte-swizzled sub-tiles the MMA descriptors expect: 8 lanes per
-    // 128-byte row slice, 4 rows per warp instruction.  Each lane's arrival
-    // on x_full fires once its copies have landed; the MMA thread fences the
-    // async proxy after that barrier.  x is read from L2 (each token's head
-    // slice is read by its top-k experts), x_perm never exists.
+    // 128-byte row slice, 4 rows per warp instruction.  Each lane waits for
+    // its own copies, fences the generic proxy against the tensor core's
+    // async-proxy reads and arrives on x_full (a fence in the MMA thread
+    // instead would sit on the tensor pipe's critical path at every tile).
+    // x is read from L2 (each token's head slice is read by its top-k
+    // experts), x_perm never exists.
     const uint64_t pol = ptx::policy_evict_last();
     const int chunk = lane & 7, rsub = lane >> 3;
     const int rbase = (warp - kFGatherWarp) * kFGatherRows;  // this warp's first tile row
@@ -428,13 +429,13 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_w13, const __grid_cons
         for (int kb = 0; kb < ksub; ++kb)
           ptx::cp_async_16(dst + static_cast<uint32_t>(kb * kFSub), src + kb * kBK, v ? 16u : 0u, pol);
       }
-      ptx::cp_async_mbar_arrive_noinc(ptx::smem_u32(&x_full));
+      // this lane's copies land, are ordered before the tensor core's
+      // (async-proxy) reads by this lane's own proxy fence, then x_full
+      ptx::cp_async_wait_all();
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(ptx::smem_u32(&x_full));
     }
-    // drain: this lane's copies land, and their barrier arrival with them
-    ptx::cp_async_wait_all();
-    const volatile int never = 0;
-    if (tiles > 0 && !ptx::mbar_wait(ptx::smem_u32(&x_full), (tiles - 1) & 1u, &never, a.wait_ns))
-      atomicOr(a.status, MOE_DEV_TIMEOUT);
+    ptx::cp_async_wait_all();  // (an early exit leaves no copy in flight)
   }
 
   ptx::tc_fence_before();

@@ -90,6 +90,12 @@ CONFIGS = {
     "headlocal": MoeConfig("headlocal", T=10752, d=3072, E=256, inter=512, head_local=True,
                            note="head-local MoE: 12 heads x 256 dims, 256 experts per head, top-6 per head, "
                                 "expert inter 512, T=10752"),
+    # not one of the pages' workloads: the head-local layer with a quarter of
+    # the experts per head and a quarter of the tokens (the same ~252 rows per
+    # expert; under 1 GB on the device), small enough for full profiler captures
+    "headlocal_slice": MoeConfig("headlocal_slice", T=2688, d=3072, E=64, inter=512, head_local=True,
+                                 note="profiling size: head-local MoE, 12 heads x 256 dims, 64 experts per head, "
+                                      "top-6 per head, expert inter 512, T=2688"),
     # not one of the pages' workloads: a 4096-token slice at clip width with 32
     # experts, small enough (~1.5 GB on the device) for full profiler captures
     "slice": MoeConfig("slice", T=4096, d=4096, E=32, inter=1024,
@@ -100,7 +106,8 @@ CONFIGS = {
     "clip_slice": MoeConfig("clip_slice", T=16384, d=4096, E=128, inter=1024, bias="zipf",
                             note="profiling size: 16384 tokens at the clip workload's width, experts and bias"),
 }
-CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "headlocal", "slice", "clip_slice"]
+CONFIG_ORDER = ["tiny", "frame", "chunk", "clip", "refiner", "chunk_mm", "headlocal", "slice", "clip_slice",
+                "headlocal_slice"]
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
