@@ -17,11 +17,13 @@
 //      128-byte-swizzled 64-column sub-tiles)
 //   3. acc2 += act_p W_down[:, 128p, 128p + 128)^T   (TMEM, D columns)
 // and at the end y = bf16(acc2).  Every MMA is 128 x 256 x 16 (both the
-// gate/up and the down products are 256 wide): with M = 128, narrower MMAs
-// run at the rate of 256-wide ones and halve the tensor pipe's throughput.
-// acc1 has one buffer (acc1 256 + acc2 256 columns fill tensor memory); the
-// eight epilogue warps read it out quickly and the MMA thread issues piece
-// p-1's down products in between, so the tensor pipe keeps running.  act is
+// gate/up and the down products are 256 wide).  acc1 has one buffer (acc1
+// 256 + acc2 256 columns fill tensor memory); the eight epilogue warps read
+// it out quickly and the MMA thread issues piece p-1's down products in
+// between, so the tensor pipe keeps running.  (A 128 x 128 x 16 MMA keeps
+// the pipe's full rate too, but 64-column pieces with two gate/up
+// accumulators, which that would allow, ran 25-35% slower: twice the
+// SwiGLU hand-offs and gate/up MMAs per tile.)  act is
 // rounded to bf16 exactly as the two separate GEMMs round it, and both
 // products run the same MMA sequence, so y has the bits of the unfused pair.
 //
