@@ -86,6 +86,7 @@ _SIGS = {
     "moe_get_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
     "moe_prepare_weights": (ctypes.c_int, [_DP, _P, _P, _P, _P]),
     "moe_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
+    "moe_selftest_timeout_fused": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint32, _P]),
     "moe_route": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_route_fused": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_route_two_stage": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -253,6 +254,12 @@ def moe_get_device_status(ws, stream=None) -> int:
 def moe_selftest_timeout(ws, limit_us: int, stream=None) -> None:
     """Runs the GEMM kernel with a loader that issues nothing (waits time out)."""
     _check(lib().moe_selftest_timeout(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)), "moe_selftest_timeout")
+
+
+def moe_selftest_timeout_fused(ws, limit_us: int, stream=None) -> None:
+    """Runs the fused head-local expert kernel with a weight loader that issues nothing."""
+    _check(lib().moe_selftest_timeout_fused(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)),
+           "moe_selftest_timeout_fused")
 
 
 def moe_prepare_weights(dims, w_gate, w_up, w13, stream=None) -> None:

@@ -88,6 +88,10 @@ struct FfnFusedArgs {
   uint16_t* y;         // [rows, D]
   int* status;
   uint64_t wait_ns;
+  // Self-test only: the weight loader issues nothing, so the MMA thread's
+  // stage wait runs out and the timeout path (status bit, abort of the
+  // other roles, drain, TMEM release) executes.
+  int selftest_stall;
 };
 
 __global__ void __launch_bounds__(kFThreads, 1)
@@ -199,7 +203,7 @@ ffn_fused_kernel(const __grid_constant__ CUtensorMap tmap_w13, const __grid_cons
       // tile's first loads)
       int g = 0, r0, r1;
       if (static_cast<int>(blockIdx.x) < n_tiles) g = decode(blockIdx.x, &r0, &r1);
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < n_tiles && ok && !a.selftest_stall; t += gridDim.x) {
         int g_n = 0;
         {
           // ring order: w13(0), w13(1), wd(0), w13(2), wd(1), ..., w13(np-1), wd(np-2), wd(np-1)
@@ -501,12 +505,26 @@ __global__ void __launch_bounds__(1024) tile_prefix_kernel(const int* __restrict
 
 bool ffn_fused_supported(int D, int I) { return D % 64 == 0 && D >= 64 && D <= kFMaxD && I % 128 == 0 && I >= 128; }
 
+namespace {
+
+int run_ffn_fused(const CUtensorMap& tw, const CUtensorMap& td, const FfnFusedArgs& fa, int grid,
+                  cudaStream_t stream) {
+  static std::atomic<uint64_t> smem_set{0};
+  if (!smem_attr_ready(ffn_fused_kernel, kFDynBytes, smem_set)) return MOE_ERR_CUDA;
+  // at most one CTA per SM; a CTA with no tile returns at once
+  ffn_fused_kernel<<<grid, kFThreads, kFDynBytes, stream>>>(tw, td, fa);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
 int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream) {
   if (!ffn_fused_supported(a.d, a.I)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.rows >= (int64_t{1} << 31) || a.T >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a.x == nullptr || a.src_token == nullptr || a.head_groups < 1 || a.x_ld < a.d || a.x_ld % 8 != 0)
     return MOE_ERR_INVALID_ARG;
   CUtensorMap tw, td;
+  // w13: 256 rows (two 64-column chunks' gate | up) per load; W_down: D rows per load
   if (!make_tmap_bf16_2d(&tw, a.w13, a.d, static_cast<uint64_t>(a.E) * 2 * a.I, kBK, 256)) return MOE_ERR_CUDA;
   if (!make_tmap_bf16_2d(&td, a.w_down, a.I, static_cast<uint64_t>(a.E) * a.d, kBK, a.d)) return MOE_ERR_CUDA;
   if (a.tiles == nullptr || a.E < 1) return MOE_ERR_INVALID_ARG;
@@ -527,11 +545,47 @@ int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream) {
   fa.y = a.y_perm;
   fa.status = a.status;
   fa.wait_ns = kWaitLimitNs;
-  static std::atomic<uint64_t> smem_set{0};
-  if (!smem_attr_ready(ffn_fused_kernel, kFDynBytes, smem_set)) return MOE_ERR_CUDA;
-  // at most one CTA per SM; a CTA with no tile returns at once
-  ffn_fused_kernel<<<a.sm_count, kFThreads, kFDynBytes, stream>>>(tw, td, fa);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return run_ffn_fused(tw, td, fa, a.sm_count, stream);
+}
+
+// The fused kernel on one 128-row tile (D = 64, I = 128, all rows reading
+// token 0) with its weight loader stalled; `scratch` holds the tile's
+// buffers (96 KB, 16-byte aligned).
+int launch_ffn_fused_selftest(uint8_t* scratch, int* status, uint64_t limit_ns, cudaStream_t stream) {
+  constexpr int D = 64, I = 128, R = 128;
+  uint16_t* x = reinterpret_cast<uint16_t*>(scratch);              // [R, D]
+  uint16_t* w13 = x + R * D;                                       // [2I, D]
+  uint16_t* wd = w13 + 2 * I * D;                                  // [D, I]
+  uint16_t* y = wd + D * I;                                        // [R, D]
+  int* src = reinterpret_cast<int*>(y + R * D);                    // [R]
+  int* offsets = src + R;                                          // [2]
+  int* tiles = offsets + 4;                                        // [2]
+  static const int kOffsets[2] = {0, R};
+  if (cudaMemsetAsync(scratch, 0, reinterpret_cast<uint8_t*>(offsets) - scratch, stream) != cudaSuccess ||
+      cudaMemcpyAsync(offsets, kOffsets, sizeof(kOffsets), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  CUtensorMap tw, td;
+  if (!make_tmap_bf16_2d(&tw, w13, D, 2 * I, kBK, 256)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&td, wd, I, D, kBK, D)) return MOE_ERR_CUDA;
+  tile_prefix_kernel<<<1, 1024, 0, stream>>>(offsets, 1, R, tiles, status);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  FfnFusedArgs fa{};
+  fa.offsets = offsets;
+  fa.tiles = tiles;
+  fa.groups = 1;
+  fa.rows = R;
+  fa.x = x;
+  fa.x_ld = D;
+  fa.src = src;
+  fa.T = R;
+  fa.head_groups = 1;
+  fa.D = D;
+  fa.I = I;
+  fa.y = y;
+  fa.status = status;
+  fa.wait_ns = limit_ns;
+  fa.selftest_stall = 1;
+  return run_ffn_fused(tw, td, fa, 1, stream);
 }
 
 }  // namespace moe

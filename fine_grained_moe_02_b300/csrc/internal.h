@@ -154,6 +154,7 @@ bool ffn_fused_supported(int D, int I);
 int launch_ffn_fused(const FfnArgs& a, cudaStream_t stream);
 int launch_combine(const CombineArgs& a, cudaStream_t stream);
 int launch_selftest_timeout(uint16_t* scratch, int* status, uint64_t limit_ns, cudaStream_t stream);
+int launch_ffn_fused_selftest(uint8_t* scratch, int* status, uint64_t limit_ns, cudaStream_t stream);
 int launch_prepare_w13(const uint16_t* w_gate, const uint16_t* w_up, uint16_t* w13, int E, int I, int d,
                        cudaStream_t stream);
 

@@ -314,6 +314,14 @@ int moe_selftest_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* str
                                  static_cast<cudaStream_t>(stream));
 }
 
+int moe_selftest_timeout_fused(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream) {
+  if (ws == nullptr || limit_us == 0 || limit_us > 10000000u) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < kAlign + (96u << 10)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_ffn_fused_selftest(at<uint8_t>(ws, kAlign), status_ptr(ws), static_cast<uint64_t>(limit_us) * 1000u,
+                                   static_cast<cudaStream_t>(stream));
+}
+
 int moe_prepare_weights(const moe_dims* dims, const moe_bf16* w_gate, const moe_bf16* w_up, moe_bf16* w13,
                         void* stream) {
   int rc = moe_check_dims(dims);

@@ -124,6 +124,15 @@ int moe_get_device_status(void* ws, int32_t* status, void* stream);
  * result with moe_get_device_status. */
 int moe_selftest_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
 
+/* The same self-test for the fused head-local expert kernel (the one
+ * moe_forward_headlocal runs): one 128-row tile, its weight loader told to
+ * issue nothing, so the tensor-core thread's stage wait runs out after
+ * limit_us microseconds (1 .. 10^7); the other roles (SwiGLU epilogue, x
+ * gather) see the abort and return, tensor memory is released, and
+ * MOE_DEV_TIMEOUT is set in the status word of `ws`.  Uses the first
+ * 1 KB + 96 KB of `ws` (ws_bytes >= 97 KB). */
+int moe_selftest_timeout_fused(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
+
 /* Builds the interleaved gate/up weight used by moe_expert_ffn:
  *   w13[e] is [2*inter, d]; for block b = 0 .. inter/64 - 1 its rows
  *   [128b, 128b+64) are w_gate[e][64b, 64b+64) and rows [128b+64, 128b+128)

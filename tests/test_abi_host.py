@@ -103,6 +103,10 @@ def test_selftest_argument_checks(L):
     assert L.moe_selftest_timeout(P, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_timeout(ctypes.c_void_p(0x10008), 1 << 20, 1000, None) == B.MOE_ERR_MISALIGNED
     assert L.moe_selftest_timeout(P, 4096, 1000, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_selftest_timeout_fused(None, 1 << 20, 1000, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_timeout_fused(P, 1 << 20, 10 ** 7 + 1, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_timeout_fused(ctypes.c_void_p(0x10008), 1 << 20, 1000, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_selftest_timeout_fused(P, 96 << 10, 1000, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_undersized_tensors_are_rejected_before_any_device_work():

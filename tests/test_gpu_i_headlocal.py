@@ -120,3 +120,19 @@ def test_fused_expert_kernel_gives_the_staged_bits(kw):
     assert torch.equal(idx, idx2)
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     _check(inp, out, idx, _)
+
+
+def test_fused_expert_kernel_wait_timeout_is_reported_and_the_context_survives():
+    # the fused kernel's weight loader issues nothing: the tensor-core
+    # thread's stage wait runs out after 20 ms, the other roles abort
+    ws = moe.alloc_workspace(1 << 20)
+    moe.moe_clear_device_status(ws)
+    moe.moe_selftest_timeout_fused(ws, 20_000)
+    assert moe.moe_get_device_status(ws) & moe.binding.MOE_DEV_TIMEOUT
+    # the GPU still runs the fused kernel correctly afterwards (tensor memory was released)
+    inp = mi.make_inputs(mi.custom_config("hlt", head_local=True, T=300, d=512, n_heads=2, head_dim=256, E=8,
+                                          inter=256, top_k=2))
+    dev = HLDev(inp)
+    out, idx, logits = dev.forward()
+    assert moe.moe_get_device_status(dev.ws) == 0
+    _check(inp, out, idx, logits)
