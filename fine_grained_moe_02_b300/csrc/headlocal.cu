@@ -42,7 +42,8 @@ struct HlLayout {
 };
 
 // Per-head arrays side by side: idx/gate/row_of/src [H, T, k], offsets [H, E+1],
-// x_perm (then y_perm) [H, T*k, head_dim], act [H, T*k, inter], dispatch
+// y_perm [H, T*k, head_dim] (the staged path's x_perm first), act [H, T*k,
+// inter] (staged path only), dispatch
 // counters [H][nblk][E]; goff [H*E + 1]: the group offsets of all heads'
 // experts over the concatenated rows (head h's rows start at h*T*k); tiles
 // [H*E + 1]: the fused expert kernel's table of the groups' tile counts.
@@ -161,9 +162,10 @@ int forward_headlocal(const moe_dims* dims, const moe_bf16* x, const moe_bf16* w
   da.sm_count = sms;
   if ((rc = launch_dispatch(da, s)) != MOE_OK) return rc;
 
-  // 3. the grouped expert GEMMs over all heads' experts at once (group h*E + e
-  //    = expert e of head h; y_perm overwrites x_perm); head by head when the
-  //    n_heads * E groups exceed the engine's table
+  // 3. both expert layers over all heads' experts at once (group h*E + e =
+  //    expert e of head h): the fused kernel (x gathered on chip, act on
+  //    chip), or the two grouped GEMMs (y_perm overwrites x_perm), head by
+  //    head when the n_heads * E groups exceed the engine's table
   FfnArgs fa{};
   fa.d = Dh;
   fa.I = I;
