@@ -192,3 +192,21 @@ def test_layer_wrapper_runs_the_entry_point_it_names(router, fuse):
         moe.moe_forward_fused(dev.dims, dev.x, dev.w_lat, dev.w_head, dev.bias, dev.w13, dev.w_down, want, fuse,
                               dev.ws)
     assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_tiny_forward_matches_the_stored_oracle_sample():
+    # the stored fp64 oracle sample (tests/golden/tiny_oracle.json, written
+    # by oracle/ only): same routing on every sampled token (all clear of
+    # near-ties) and the sampled outputs within the layer's bars
+    import json
+    import pathlib
+    g = json.loads((pathlib.Path(__file__).resolve().parent / "golden" / "tiny_oracle.json").read_text())
+    inp = mi.make_inputs("tiny")
+    dev = G.Dev(inp)
+    idx, _, _ = dev.route(want_logits=False)
+    out = G.host_f64(dev.forward())
+    assert dev.status() == 0
+    t = g["tokens"]
+    assert min(g["topk_gap"]) > 2e-3
+    np.testing.assert_array_equal(idx.cpu().numpy()[t], np.array(g["topk_idx"]))
+    G.check_out(out[t, :g["out_cols"]], np.array(g["out"]))
