@@ -95,9 +95,10 @@ def _m_combine_ignores_gates(m):
 
 def _m_softmax_wrong_axis(m):
     def sm(s):
-        z = s - s.max(axis=0, keepdims=True)
-        ez = np.exp(z)
-        return ez / ez.sum(axis=0, keepdims=True)
+        with np.errstate(invalid="ignore", over="ignore"):   # the mutant may meet inf - inf
+            z = s - s.max(axis=0, keepdims=True)
+            ez = np.exp(z)
+            return ez / ez.sum(axis=0, keepdims=True)
     m.softmax = sm
 
 
