@@ -668,7 +668,7 @@ def main():
         "gemm1_tflops": g1_tf, "gemm2_tflops": g2_tf,
         "router_tflops": alg["router_flops"] / (stage_ms["route"] * 1e-3) / 1e12,
         "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / pk["hbm"],
-        "permute_note": "dispatch stage (histogram, scan, rank assignment and the row gather)",
+        "permute_note": "dispatch stage (histogram, rank assignment with the in-block scan, row gather)",
         "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / pk["hbm"],
         "roofline": {"kernel": "expert GEMM-1 + SwiGLU (gemm_tc_kernel<256, EpiSwiGLU>)", "bound": "tensor",
                      "achieved": g1_tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": g1_tf / pk["bf16_sus"],
