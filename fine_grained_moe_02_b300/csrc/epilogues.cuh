@@ -66,6 +66,17 @@ __device__ __forceinline__ void store_rows64(EpiCtx& ctx, int row0w, int col0, i
   }
 }
 
+// Waits ctx.store_delay cycles (see EpiCtx) before a store-heavy epilogue's
+// first store.  Expert GEMM-2 writes 64 KB per 128 x 256 tile against eight
+// times less for GEMM-1; storing right when a tile's MMAs finish collides
+// with the next tile's first operand loads.  On the clip workload, waiting
+// half a tile's MMA time took GEMM-2 from 0.83 to 0.87 TFLOP/s per SM MHz.
+__device__ __forceinline__ void store_delay_wait(const EpiCtx& ctx) {
+  if (ctx.store_delay == 0) return;
+  const long long t0 = clock64();
+  while (clock64() - t0 < static_cast<long long>(ctx.store_delay)) __nanosleep(128);
+}
+
 // Hands the accumulator back to the MMA warp.  The caller's tcgen05.ld's have
 // completed (tmem_ld32 waits on them), so the next tile's MMAs may overwrite
 // the columns while this warp's stores of the tile are still under way.
@@ -125,6 +136,7 @@ struct EpiStoreBf16 {
       for (int j = 0; j < 16; ++j) pk[col / 2 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     }
     release_accumulator(ctx);
+    store_delay_wait(ctx);
     if (nvalid > 0) {
 #pragma unroll
       for (int col = 0; col < BN; col += 64)
@@ -177,6 +189,7 @@ struct EpiStoreGated {
       for (int j = 0; j < 16; ++j) pk[col / 2 + j] = pack_bf16x2(gw * v[2 * j], gw * v[2 * j + 1]);
     }
     release_accumulator(ctx);
+    store_delay_wait(ctx);
     if (nvalid > 0) {
 #pragma unroll
       for (int col = 0; col < BN; col += 64)

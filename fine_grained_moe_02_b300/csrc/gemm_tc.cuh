@@ -121,6 +121,11 @@ struct EpiCtx {
   const volatile int* abort;
   uint64_t wait_ns;
   bool failed;
+  // cycles a store-heavy epilogue waits between handing the accumulator back
+  // and its first store (0 on the CTA's last tile): half the next tile's MMA
+  // time, so the tile's stores meet the next tile's operand loads mid-way
+  // rather than at its start
+  uint32_t store_delay;
 };
 
 struct TileCoord {
@@ -426,7 +431,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     EpiCtx ctx{&tmap_d, ptx::smem_u32(smem + STAGES * S::kStageBytes + quad * kOutChunkBytes), lane, quad, false,
                0u, false, (warp - 2) / 4, ptx::smem_u32(smem + STAGES * S::kStageBytes),
-               ptx::smem_u32(&hand_bar[quad]), ptx::smem_u32(&hand_bar[4 + quad]), 0u, &s_abort, wait_ns, false};
+               ptx::smem_u32(&hand_bar[quad]), ptx::smem_u32(&hand_bar[4 + quad]), 0u, &s_abort, wait_ns, false, 0u};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = first_tile; tile < total; tile += tile_step) {
@@ -440,6 +445,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
       ctx.tempty = ptx::smem_u32(&tempty_bar[acc]);
       ctx.released = false;
+      // a k-slice of 128 x BN x 64 MMAs takes 2*BN cycles at the pipe's rate
+      ctx.store_delay = tile + tile_step < total ? static_cast<uint32_t>(num_kb * BN) : 0u;
       // an epilogue may hand the accumulator back itself (release_accumulator)
       // as soon as it holds the tile in registers, before its stores
       Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile, ctx);
