@@ -70,7 +70,8 @@ __device__ __forceinline__ void store_rows64(EpiCtx& ctx, int row0w, int col0, i
 // first store.  Expert GEMM-2 writes 64 KB per 128 x 256 tile against eight
 // times less for GEMM-1; storing right when a tile's MMAs finish collides
 // with the next tile's first operand loads.  On the clip workload, waiting
-// half a tile's MMA time took GEMM-2 from 0.83 to 0.87 TFLOP/s per SM MHz.
+// half a tile's MMA time took GEMM-2 from 0.83 to 0.875 TFLOP/s per SM MHz,
+// spreading the four warps' waits over 0.25-0.7 of it to 0.89.
 __device__ __forceinline__ void store_delay_wait(const EpiCtx& ctx) {
   if (ctx.store_delay == 0) return;
   const long long t0 = clock64();

@@ -122,9 +122,9 @@ struct EpiCtx {
   uint64_t wait_ns;
   bool failed;
   // cycles a store-heavy epilogue waits between handing the accumulator back
-  // and its first store (0 on the CTA's last tile): half the next tile's MMA
-  // time, so the tile's stores meet the next tile's operand loads mid-way
-  // rather than at its start
+  // and its first store (0 on the CTA's last tile): a quarter to 0.7 of the
+  // next tile's MMA time, by lane quadrant, so the tile's stores are spread
+  // over the next tile's operand loads rather than meeting their start
   uint32_t store_delay;
 };
 
@@ -445,8 +445,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant
       const TileCoord c = decode_tile<BN>(tile, rows, s_tile, groups, n_tiles);
       ctx.tempty = ptx::smem_u32(&tempty_bar[acc]);
       ctx.released = false;
-      // a k-slice of 128 x BN x 64 MMAs takes 2*BN cycles at the pipe's rate
-      ctx.store_delay = tile + tile_step < total ? static_cast<uint32_t>(num_kb * BN) : 0u;
+      // a k-slice of 128 x BN x 64 MMAs takes 2*BN cycles at the pipe's rate,
+      // so num_kb * BN is half the tile's MMA time; the four lane quadrants
+      // start their stores at 0.25, 0.4, 0.55 and 0.7 of it
+      ctx.store_delay = tile + tile_step < total ? static_cast<uint32_t>(num_kb * BN * (5 + 3 * quad) / 10) : 0u;
       // an epilogue may hand the accumulator back itself (release_accumulator)
       // as soon as it holds the tile in registers, before its stores
       Epi::template run<BN>(ep, c, lane_addr + static_cast<uint32_t>(acc * S::kAccStride), row_in_tile, ctx);
